@@ -1,0 +1,286 @@
+/*
+ * pkv.h - C ABI of libpkv.so, PagedAttention over a flattened, variable-length
+ * token batch on one NVIDIA GB300 (sm_103a).
+ *
+ * Pages cited (by title and section):
+ *   [AI Infra]  "AI Infra入门干货总结：大模型是如何高效推理的"
+ *   [抢占]      "vLLM 抢占机制源码精读"
+ *   [调度实战]  "GPT-5 时代大模型推理调度系统深度实战"
+ *   [Chunked]   "Chunked Prefill 与 Preemption"
+ *   [显存调度]  "显存与调度" (book chapter 32)
+ *
+ * Conventions shared by every entry point
+ *   - Return value: PKV_OK (0) on success, a negative PKV_E_* code otherwise;
+ *     pkv_last_error() returns a message for the calling thread's last error.
+ *     No C++ exception crosses this interface and no kernel traps.
+ *   - Device entry points take DEVICE pointers owned by the caller and a
+ *     cudaStream_t passed as `void* stream` (NULL = the legacy default
+ *     stream).  They enqueue work asynchronously, never synchronise the
+ *     stream and never allocate or free device memory.
+ *   - Host entry points (allocator, scheduler, metadata) take HOST pointers;
+ *     opaque handles are owned by the library and released by *_destroy.
+ *   - Float tensors are all float32 (PKV_F32) or all bfloat16 (PKV_BF16)
+ *     within one call.  Index arrays are int32 except slot_mapping (int64).
+ *   - Cache layout [AI Infra, section "Paged Attention"]: one layer's key
+ *     cache and value cache are each [num_blocks, block_size, num_kv_heads,
+ *     head_dim], contiguous, 16-byte aligned.  block_size must be 16;
+ *     head_dim 64 or 128; num_heads a multiple of num_kv_heads.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_OK 0
+#define PKV_E_INVALID (-1)      /* null pointer, bad size, stride or alignment */
+#define PKV_E_UNSUPPORTED (-2)  /* a shape or dtype this build does not handle */
+#define PKV_E_WORKSPACE (-3)    /* workspace missing or too small */
+#define PKV_E_NO_BLOCKS (-4)    /* allocator: not enough free blocks */
+#define PKV_E_STATE (-5)        /* allocator/scheduler call in the wrong state */
+#define PKV_E_UNKNOWN_REQ (-6)  /* request id not known */
+#define PKV_E_CUDA (-7)         /* a CUDA runtime call or launch failed */
+#define PKV_E_CAPACITY (-8)     /* a request would exceed its block-table row */
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits the kernels set in a caller-visible device error word instead of
+ * faulting; the offending access is skipped (reads yield zeros). */
+#define PKV_ERR_BLOCK_ID 1u     /* block_table entry outside [0, num_blocks) */
+#define PKV_ERR_SLOT 2u         /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_ERR_METADATA 4u     /* seq_len != num_computed + query_len, or a
+                                   request longer than its block-table row */
+#define PKV_ERR_TIMEOUT 8u      /* a bounded wait inside a kernel gave up */
+
+const char* pkv_last_error(void);
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------
+ * reshape_and_cache  [AI Infra, section "Paged Attention" (slot_idx rule)
+ * and section "Attention Module" (QKV split -> RoPE -> reshape_and_cache
+ * scatters the new K/V into the paged cache by slot_mapping)]
+ *
+ * For every token t < num_tokens with s = slot_mapping[t] >= 0:
+ *   key_cache  [s / block_size][s % block_size][:][:] = key  [t][:][:]
+ *   value_cache[s / block_size][s % block_size][:][:] = value[t][:][:]
+ * A negative slot marks a padding token and is skipped.  A slot >=
+ * num_blocks * block_size is skipped and sets PKV_ERR_SLOT in *error_word
+ * (if error_word is not NULL).  The copy is bit-exact.
+ *
+ * key, value: device, [num_tokens, num_kv_heads, head_dim]; token t starts at
+ *   element t * key_stride (value_stride); heads and dims are contiguous.
+ *   Strides in elements; row bytes and strides must be multiples of 16 bytes.
+ * key_cache, value_cache: device, layout above.
+ * slot_mapping: device int64 [num_tokens].
+ * error_word: device uint32 or NULL (bits are OR-ed in, never cleared).
+ * ---------------------------------------------------------------------- */
+int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
+                          int64_t value_stride, void* key_cache, void* value_cache,
+                          const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                          int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t dtype, uint32_t* error_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * paged_attention_varlen  [AI Infra, section "Attention Module (以标准GQA +
+ * RoPE为例)": attention per request over its whole K/V history read through
+ * block_table, requests separated by query_start_loc (cu_seqlens); Flash-
+ * Decoding split-KV with log-sum-exp merge; Chunked, section "Chunked
+ * Prefill：改变调度粒度，不改变 causal 结果": a chunk [a, b) sees keys j <= i]
+ *
+ * For request r with query rows t in [query_start_loc[r], query_start_loc[r+1])
+ * the row's absolute position is p = num_computed_tokens[r] + (t -
+ * query_start_loc[r]); for each query head h, with G = num_heads /
+ * num_kv_heads and KV head g = h / G:
+ *   out[t][h] = sum_{j <= p} softmax_j(scale * <q[t][h], K_r[j][g]>) V_r[j][g]
+ * where K_r[j] is the cache row at slot block_table[r][j / block_size] *
+ * block_size + j % block_size.  seq_lens[r] must equal num_computed_tokens[r]
+ * + query length (the KV length after this step's reshape_and_cache), so the
+ * keys of this step's own tokens must already be in the cache.
+ * Requests with query length 1 run on the split-KV decode kernel, longer ones
+ * on the chunked-prefill kernel; query length 0 contributes no rows.
+ *
+ * q, out: device [num_tokens, num_heads, head_dim], token stride q_stride /
+ *   out_stride elements, heads and dims contiguous.
+ * block_table: device int32 [num_reqs, block_table_stride], row-major; only
+ *   the first ceil(seq_lens[r] / block_size) entries of row r are read.
+ * query_start_loc: device int32 [num_reqs + 1], non-decreasing, [0] = 0,
+ *   [num_reqs] = num_tokens.  seq_lens, num_computed_tokens: device int32
+ *   [num_reqs].
+ * max_query_len: host hint, >= every request's query length, or 0 if
+ *   unknown; a value <= 1 skips the prefill launch.
+ * workspace: device scratch of at least pkv_attention_workspace_bytes()
+ *   bytes, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves it ready for
+ *   the next one.  Word 0 is the error word (PKV_ERR_* bits, OR-ed in).  Two
+ *   calls that overlap on the GPU must not share a workspace.
+ * ---------------------------------------------------------------------- */
+size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_t head_dim);
+
+int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_cache,
+                               const void* value_cache, const int32_t* block_table,
+                               int32_t block_table_stride, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                               float scale, void* out, int64_t out_stride, int64_t num_tokens,
+                               int32_t num_reqs, int64_t num_blocks, int32_t block_size,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t dtype, int32_t max_query_len, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Step metadata (host)  [AI Infra, section "Paged Attention": slot_idx =
+ * block_table[r][pos // block_size] * block_size + pos % block_size]
+ *
+ * slot_mapping[t] for every token of the flattened batch, requests in order:
+ * request r's tokens sit at positions num_computed_tokens[r] + k, k <
+ * query_start_loc[r+1] - query_start_loc[r].  All pointers are host memory;
+ * block_table is [num_reqs, block_table_stride].  Returns PKV_E_INVALID if a
+ * position's logical block is outside the row or num_tokens disagrees with
+ * query_start_loc[num_reqs].
+ * ---------------------------------------------------------------------- */
+int pkv_build_slot_mapping(const int32_t* block_table, int32_t block_table_stride,
+                           const int32_t* query_start_loc, const int32_t* num_computed_tokens,
+                           int32_t num_reqs, int32_t block_size, int64_t* slot_mapping,
+                           int64_t num_tokens);
+
+/* ------------------------------------------------------------------------
+ * Block allocator (host)  [显存调度, section "分配是词元计划的一部分" and
+ * Fig. 32.2: reserve all new blocks of a plan atomically, execute, then
+ * commit; failure or cancellation rolls the reservation back;
+ * q_free + q_reserved + q_committed = q_capacity after every transition;
+ * delta_q_i = ceil((T_i + s_i) / B) - ceil(T_i / B); section "从保留词元到物理块":
+ * q_i = ceil(T_i / B), w_i = q_i B - T_i.  调度实战, section 5.3: the free list
+ * is drained from its front and refilled at its back.]
+ *
+ * Blocks are ids 0..num_blocks-1; the free list starts in that order.
+ * reserve() takes n (request id, new token count) pairs, computes each
+ * request's delta_q_i from its committed token count T_i and either takes all
+ * blocks (from the front of the free list, in pair order) or none
+ * (PKV_E_NO_BLOCKS, state unchanged).  commit() makes the reservation part of
+ * each request's table and adds s_i to T_i; rollback() returns the reserved
+ * blocks to the front of the free list so it is exactly as before.
+ * free_request() releases a request's committed blocks (block-table order),
+ * then any of its reserved ones, to the back of the free list.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_alloc pkv_alloc;
+
+typedef struct {
+  int64_t capacity;        /* q_capacity */
+  int64_t free;            /* q_free */
+  int64_t reserved;        /* q_reserved (open plan) */
+  int64_t committed;       /* q_committed */
+  int64_t num_requests;    /* requests holding committed blocks */
+  int64_t tail_waste;      /* sum of w_i over committed requests, in token slots */
+  int64_t alloc_failures;  /* reserve() calls refused for lack of blocks */
+  int64_t peak_used;       /* highest reserved + committed seen */
+} pkv_alloc_stats;
+
+pkv_alloc* pkv_alloc_create(int32_t num_blocks, int32_t block_size, int32_t max_blocks_per_req);
+void pkv_alloc_destroy(pkv_alloc* a);
+int pkv_alloc_reserve(pkv_alloc* a, int32_t n, const int32_t* req_ids, const int32_t* new_tokens);
+int pkv_alloc_commit(pkv_alloc* a);
+int pkv_alloc_rollback(pkv_alloc* a);
+/* returns the number of blocks released (>= 0) or an error */
+int pkv_alloc_free_request(pkv_alloc* a, int32_t req_id);
+int pkv_alloc_get_stats(const pkv_alloc* a, pkv_alloc_stats* out);
+/* committed + reserved blocks of req_id into out[0..capacity); returns the
+ * count (0 for an unknown request) or an error if capacity is too small */
+int pkv_alloc_table(const pkv_alloc* a, int32_t req_id, int32_t* out, int32_t capacity);
+/* T_i: committed token count of req_id (0 if unknown) */
+int64_t pkv_alloc_held_tokens(const pkv_alloc* a, int32_t req_id);
+/* the free list, front first; returns its length or an error */
+int pkv_alloc_free_list(const pkv_alloc* a, int32_t* out, int32_t capacity);
+/* verifies conservation, q_i = ceil(T_i / B), and that every block id is in
+ * exactly one place; PKV_OK or PKV_E_STATE */
+int pkv_alloc_check(const pkv_alloc* a);
+
+/* ------------------------------------------------------------------------
+ * Continuous-batching scheduler (host)  [AI Infra, sections "连续批处理" and
+ * "附4：vLLM调度详细流程"; 抢占, sections "抢占的触发条件", "_schedule_running 中
+ * 的抢占循环", "reset_state_for_recompute 的巧妙设计", "人工抢占测试"; 显存调度,
+ * sections "分配是词元计划的一部分" and "分块预填充共享每轮预算"]
+ *
+ * One step: RUNNING requests head first get s_i = min(num_tokens -
+ * num_computed, chunk_size, remaining budget); when a request's new blocks do
+ * not fit, the tail of RUNNING is preempted by recompute (blocks freed,
+ * num_computed = 0, moved to the front of WAITING) until it fits, or the
+ * request preempts itself when it is the tail and the scan stops.  Only in a
+ * step without preemption are WAITING requests admitted, head first, while
+ * RUNNING < max_num_seqs, budget remains and their first chunk fits.  All new
+ * blocks are then reserved at once (plan order).  finish_step(1) commits:
+ * num_computed += s_i; a request that caught up samples one token and
+ * either finishes (blocks freed) or grows num_tokens by one.
+ * finish_step(0) rolls the reservation back.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_sched pkv_sched;
+
+typedef struct {
+  int32_t max_num_seqs;
+  int32_t max_num_batched_tokens;   /* token budget K per step */
+  int32_t chunk_size;               /* largest s_i per request per step */
+  int32_t max_model_len;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_req;
+  int32_t artificial_preempt_max;   /* test hook: at most this many forced failures */
+  double artificial_preempt_prob;   /* test hook: 0 disables it */
+  uint64_t artificial_seed;         /* splitmix64 seed of the test hook */
+} pkv_sched_config;
+
+typedef struct {
+  int32_t num_reqs;       /* requests in the plan */
+  int32_t num_preempted;
+  int32_t num_admitted;
+  int32_t max_blocks;     /* longest block-table row among planned requests */
+  int64_t num_tokens;     /* sum of s_i */
+  int32_t max_query_len;  /* largest s_i */
+  int32_t pad_;
+} pkv_step_info;
+
+typedef struct {
+  int32_t status;         /* 0 waiting, 1 running, 2 finished, -1 unknown */
+  int32_t prompt_len;
+  int32_t max_output;
+  int32_t outputs;
+  int64_t num_tokens;
+  int64_t num_computed;
+  int32_t preemptions;
+  int32_t pad_;
+} pkv_request_state;
+
+pkv_sched* pkv_sched_create(const pkv_sched_config* cfg);
+void pkv_sched_destroy(pkv_sched* s);
+/* 1 accepted, 0 rejected (duplicate id, prompt >= max_model_len, or a
+ * footprint that can never fit); the output target is clamped to
+ * max_model_len - prompt_len */
+int pkv_sched_add_request(pkv_sched* s, int32_t req_id, int32_t prompt_len, int32_t max_output);
+int pkv_sched_step(pkv_sched* s, pkv_step_info* info);
+/* plan entries, in batch order */
+int pkv_sched_plan(const pkv_sched* s, int32_t* req_ids, int32_t* num_new_tokens,
+                   int32_t* num_computed_before, int32_t capacity);
+int pkv_sched_preempted(const pkv_sched* s, int32_t* out, int32_t capacity);
+int pkv_sched_admitted(const pkv_sched* s, int32_t* out, int32_t capacity);
+/* the open step's kernel inputs, requests in plan order: block_table rows
+ * (committed + reserved blocks, unused entries -1), query_start_loc [R+1],
+ * seq_lens [R], num_computed_tokens [R], slot_mapping [num_tokens]; host
+ * buffers, block_table_stride >= info.max_blocks */
+int pkv_sched_build_metadata(const pkv_sched* s, int32_t* block_table, int32_t block_table_stride,
+                             int32_t* query_start_loc, int32_t* seq_lens,
+                             int32_t* num_computed_tokens, int64_t* slot_mapping);
+/* commit (executed_ok != 0) or roll back; finished request ids go to
+ * finished[0..capacity); returns how many finished */
+int pkv_sched_finish_step(pkv_sched* s, int32_t executed_ok, int32_t* finished, int32_t capacity);
+int pkv_sched_request(const pkv_sched* s, int32_t req_id, pkv_request_state* out);
+int pkv_sched_queues(const pkv_sched* s, int32_t* running, int32_t* num_running, int32_t* waiting,
+                     int32_t* num_waiting, int32_t capacity);
+/* counters: [0] total preemptions, [1] recomputed tokens, [2] finished requests,
+ * [3] remaining artificial failures */
+int pkv_sched_counters(const pkv_sched* s, int64_t* out4);
+const pkv_alloc* pkv_sched_allocator(const pkv_sched* s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H_ */

@@ -37,7 +37,7 @@ class Stats:
     free: int
     reserved: int
     committed: int
-    num_requests: int
+    num_requests: int        # requests holding at least one committed block
     tail_waste: int          # sum over requests of w_i for their committed tokens
     alloc_failures: int      # reserve calls refused for lack of blocks
     peak_used: int           # max over time of reserved + committed
@@ -77,7 +77,8 @@ class NaiveAllocator:
         reserved = sum(len(n) for _, _, n in self.pending or [])
         committed = sum(len(t) for t in self.tables.values())
         waste = sum(len(self.tables[r]) * self.block_size - self.tokens[r] for r in self.tables)
-        return Stats(self.capacity, len(self.free_list), reserved, committed, len(self.tables),
+        holding = sum(1 for t in self.tables.values() if t)
+        return Stats(self.capacity, len(self.free_list), reserved, committed, holding,
                      waste, self.alloc_failures, self.peak_used)
 
     def check(self) -> None:

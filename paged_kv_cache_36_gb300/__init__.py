@@ -1,0 +1,295 @@
+"""PagedAttention over a flattened, variable-length token batch on one GB300.
+
+Thin Python binding of libpkv.so: every function marshals arguments into the
+C ABI declared in include/pkv.h and calls it; all computation runs in the
+library (CUDA kernels for sm_103a, C++ host code).  PyTorch is used only to
+hand over device pointers and the current CUDA stream.  If the library is not
+built, importing the binding's entry points raises ImportError.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from . import _ffi
+from ._ffi import (ERR_BLOCK_ID, ERR_METADATA, ERR_SLOT, ERR_TIMEOUT, PKV_BF16,  # noqa: F401
+                   PKV_F32)
+
+__all__ = [
+    "PkvError", "lib", "reshape_and_cache", "attention_workspace_bytes", "new_workspace",
+    "paged_attention_varlen", "read_error_word", "build_slot_mapping", "Allocator", "Scheduler",
+]
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = _ffi.load()
+    return _lib
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = lib().pkv_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {_ffi.ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _check(code: int, where: str) -> int:
+    if code < 0:
+        raise PkvError(code, where)
+    return code
+
+
+# ---------------------------------------------------------------------------
+# device entry points (torch tensors in, no computation here)
+# ---------------------------------------------------------------------------
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return PKV_F32
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream_ptr(stream) -> int | None:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _token_stride(t) -> int:
+    # [tokens, heads, dim] with heads and dim contiguous
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("expected [tokens, heads, head_dim] with contiguous heads and dims")
+    return t.stride(0)
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, error_word=None,
+                      stream=None) -> None:
+    """Scatter key/value [T, Hkv, D] into the caches [NB, B, Hkv, D] at slot_mapping[T] (int64)."""
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    nb, bs, hkv, d = key_cache.shape
+    code = lib().pkv_reshape_and_cache(
+        key.data_ptr(), value.data_ptr(), _token_stride(key), _token_stride(value),
+        key_cache.data_ptr(), value_cache.data_ptr(), slot_mapping.data_ptr(),
+        int(slot_mapping.shape[0]), nb, bs, hkv, d, _dtype_code(key_cache),
+        error_word.data_ptr() if error_word is not None else None, _stream_ptr(stream))
+    _check(code, "reshape_and_cache")
+
+
+def attention_workspace_bytes(num_reqs: int, num_heads: int, head_dim: int) -> int:
+    return int(lib().pkv_attention_workspace_bytes(num_reqs, num_heads, head_dim))
+
+
+def new_workspace(num_reqs: int, num_heads: int, head_dim: int, device="cuda"):
+    """A zero-filled workspace large enough for batches of up to num_reqs requests."""
+    import torch
+    n = attention_workspace_bytes(num_reqs, num_heads, head_dim)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def read_error_word(workspace) -> int:
+    """The PKV_ERR_* bits the kernels recorded in this workspace (synchronises)."""
+    return int(workspace[:4].view(dtype=__import__("torch").int32).item()) & 0xFFFFFFFF
+
+
+def paged_attention_varlen(q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
+                           num_computed_tokens, scale: float, out=None, workspace=None,
+                           max_query_len: int = 0, stream=None):
+    """Causal GQA attention of the flattened batch q [T, H, D] over the paged caches.
+
+    block_table int32 [R, max_blocks]; query_start_loc int32 [R + 1]; seq_lens,
+    num_computed_tokens int32 [R].  Returns out [T, H, D].
+    """
+    import torch
+    T, H, D = q.shape
+    nb, bs, hkv, d2 = key_cache.shape
+    R = int(seq_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = new_workspace(R, H, D, q.device)
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [R, max_blocks] with unit inner stride")
+    code = lib().pkv_paged_attention_varlen(
+        q.data_ptr(), _token_stride(q), key_cache.data_ptr(), value_cache.data_ptr(),
+        block_table.data_ptr(), block_table.stride(0), query_start_loc.data_ptr(),
+        seq_lens.data_ptr(), num_computed_tokens.data_ptr(), float(scale), out.data_ptr(),
+        _token_stride(out), T, R, nb, bs, H, hkv, D, _dtype_code(q), int(max_query_len),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(code, "paged_attention_varlen")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# host entry points (numpy arrays)
+# ---------------------------------------------------------------------------
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def build_slot_mapping(block_table: np.ndarray, query_start_loc, num_computed_tokens,
+                       block_size: int) -> np.ndarray:
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    nc = np.ascontiguousarray(num_computed_tokens, dtype=np.int32)
+    n = int(qsl[-1]) if len(qsl) else 0
+    out = np.empty(n, dtype=np.int64)
+    _check(lib().pkv_build_slot_mapping(_ptr(bt), bt.shape[1], _ptr(qsl), _ptr(nc), len(nc),
+                                        block_size, _ptr(out), n), "build_slot_mapping")
+    return out
+
+
+class Allocator:
+    """Reserve / commit / rollback block allocator (host)."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_req: int | None = None,
+                 _handle=None):
+        self._own = _handle is None
+        self.num_blocks = num_blocks
+        self._h = _handle or lib().pkv_alloc_create(num_blocks, block_size,
+                                                    max_blocks_per_req or num_blocks)
+        if not self._h:
+            raise PkvError(-1, "pkv_alloc_create")
+
+    def __del__(self):
+        if getattr(self, "_own", False) and self._h:
+            lib().pkv_alloc_destroy(self._h)
+            self._h = None
+
+    def reserve(self, plan) -> bool:
+        """plan: [(req_id, new_tokens)].  False if the blocks are not there."""
+        ids = np.array([r for r, _ in plan], dtype=np.int32)
+        toks = np.array([s for _, s in plan], dtype=np.int32)
+        code = lib().pkv_alloc_reserve(self._h, len(ids), _ptr(ids), _ptr(toks))
+        if code == -4:
+            return False
+        _check(code, "reserve")
+        return True
+
+    def commit(self):
+        _check(lib().pkv_alloc_commit(self._h), "commit")
+
+    def rollback(self):
+        _check(lib().pkv_alloc_rollback(self._h), "rollback")
+
+    def free_request(self, req: int) -> int:
+        return _check(lib().pkv_alloc_free_request(self._h, req), "free_request")
+
+    def stats(self) -> dict:
+        s = _ffi.AllocStats()
+        _check(lib().pkv_alloc_get_stats(self._h, C.byref(s)), "stats")
+        return {n: getattr(s, n) for n, _ in s._fields_}
+
+    def table(self, req: int) -> list[int]:
+        buf = np.empty(self.num_blocks, dtype=np.int32)
+        n = _check(lib().pkv_alloc_table(self._h, req, _ptr(buf), len(buf)), "table")
+        return buf[:n].tolist()
+
+    def held_tokens(self, req: int) -> int:
+        return int(lib().pkv_alloc_held_tokens(self._h, req))
+
+    def free_list(self) -> list[int]:
+        buf = np.empty(self.num_blocks, dtype=np.int32)
+        n = _check(lib().pkv_alloc_free_list(self._h, _ptr(buf), len(buf)), "free_list")
+        return buf[:n].tolist()
+
+    def check(self):
+        _check(lib().pkv_alloc_check(self._h), "check")
+
+
+class Scheduler:
+    """Continuous-batching scheduler with recompute preemption (host)."""
+
+    def __init__(self, max_num_seqs, max_num_batched_tokens, chunk_size, max_model_len,
+                 block_size, num_blocks, max_blocks_per_req, artificial_preempt_prob=0.0,
+                 artificial_preempt_max=0, artificial_seed=0):
+        cfg = _ffi.SchedConfig(max_num_seqs, max_num_batched_tokens, chunk_size, max_model_len,
+                               block_size, num_blocks, max_blocks_per_req, artificial_preempt_max,
+                               artificial_preempt_prob, artificial_seed)
+        self._h = lib().pkv_sched_create(C.byref(cfg))
+        if not self._h:
+            raise PkvError(-1, "pkv_sched_create")
+        self.num_blocks = num_blocks
+        self.max_blocks_per_req = max_blocks_per_req
+        self.allocator = Allocator(num_blocks, block_size, _handle=lib().pkv_sched_allocator(self._h))
+        self.info = _ffi.StepInfo()
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            lib().pkv_sched_destroy(self._h)
+            self._h = None
+
+    def add_request(self, req_id: int, prompt_len: int, max_output: int) -> bool:
+        return bool(_check(lib().pkv_sched_add_request(self._h, req_id, prompt_len, max_output),
+                           "add_request"))
+
+    def step(self) -> dict:
+        _check(lib().pkv_sched_step(self._h, C.byref(self.info)), "step")
+        i = self.info
+        n = i.num_reqs
+        ids = np.empty(n, np.int32)
+        toks = np.empty(n, np.int32)
+        before = np.empty(n, np.int32)
+        lib().pkv_sched_plan(self._h, _ptr(ids), _ptr(toks), _ptr(before), n)
+        pre = np.empty(max(i.num_preempted, 1), np.int32)
+        adm = np.empty(max(i.num_admitted, 1), np.int32)
+        lib().pkv_sched_preempted(self._h, _ptr(pre), len(pre))
+        lib().pkv_sched_admitted(self._h, _ptr(adm), len(adm))
+        return {"entries": list(zip(ids.tolist(), toks.tolist(), before.tolist())),
+                "preempted": pre[:i.num_preempted].tolist(), "admitted": adm[:i.num_admitted].tolist(),
+                "num_tokens": int(i.num_tokens), "max_blocks": int(i.max_blocks),
+                "max_query_len": int(i.max_query_len)}
+
+    def build_metadata(self, block_table, query_start_loc, seq_lens, num_computed, slot_mapping):
+        """Fill caller-owned numpy buffers (e.g. views of pinned host tensors)."""
+        _check(lib().pkv_sched_build_metadata(
+            self._h, _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
+            _ptr(seq_lens), _ptr(num_computed), _ptr(slot_mapping)), "build_metadata")
+
+    def metadata(self, stride: int | None = None):
+        i = self.info
+        stride = stride or max(int(i.max_blocks), 1)
+        bt = np.empty((i.num_reqs, stride), np.int32)
+        qsl = np.empty(i.num_reqs + 1, np.int32)
+        seq = np.empty(i.num_reqs, np.int32)
+        nc = np.empty(i.num_reqs, np.int32)
+        slots = np.empty(int(i.num_tokens), np.int64)
+        self.build_metadata(bt, qsl, seq, nc, slots)
+        return bt, qsl, seq, nc, slots
+
+    def finish_step(self, executed_ok: bool) -> list[int]:
+        buf = np.empty(1024, np.int32)
+        n = _check(lib().pkv_sched_finish_step(self._h, 1 if executed_ok else 0, _ptr(buf),
+                                               len(buf)), "finish_step")
+        return buf[:min(n, len(buf))].tolist()
+
+    def request(self, req_id: int) -> dict | None:
+        st = _ffi.RequestState()
+        code = lib().pkv_sched_request(self._h, req_id, C.byref(st))
+        if code == -6:
+            return None
+        _check(code, "request")
+        return {n: getattr(st, n) for n, _ in st._fields_ if n != "pad_"}
+
+    def queues(self):
+        cap = 1 << 16
+        run = np.empty(cap, np.int32)
+        wait = np.empty(cap, np.int32)
+        nr, nw = C.c_int32(0), C.c_int32(0)
+        _check(lib().pkv_sched_queues(self._h, _ptr(run), C.byref(nr), _ptr(wait), C.byref(nw),
+                                      cap), "queues")
+        return run[:nr.value].tolist(), wait[:nw.value].tolist()
+
+    def counters(self) -> dict:
+        out = (C.c_int64 * 4)()
+        _check(lib().pkv_sched_counters(self._h, out), "counters")
+        return {"preemptions": out[0], "recomputed_tokens": out[1], "finished": out[2],
+                "inject_left": out[3]}

@@ -1,0 +1,210 @@
+// C ABI of the device entry points: argument checks, workspace layout, TMA
+// descriptors and kernel launches.  See include/pkv.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "pkv_error.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kVersion = 1;
+constexpr size_t kHeaderBytes = 256;  // error word + padding
+constexpr int64_t kMaxTmaRows = 0x7fffffffLL;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct WorkspaceLayout {
+  size_t counters, part_ml, part_o, total;
+  int64_t slots;
+};
+
+WorkspaceLayout workspace_layout(int32_t num_reqs, int32_t num_heads, int32_t head_dim, int grid) {
+  WorkspaceLayout w;
+  w.slots = static_cast<int64_t>(grid) + num_reqs;
+  w.counters = kHeaderBytes;
+  w.part_ml = w.counters + align256(sizeof(int32_t) * static_cast<size_t>(num_reqs) * num_heads);
+  w.part_o = w.part_ml + align256(sizeof(float) * 2 * static_cast<size_t>(w.slots) * num_heads);
+  w.total = w.part_o + align256(sizeof(float) * static_cast<size_t>(w.slots) * num_heads * head_dim);
+  return w;
+}
+
+int current_grid() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  return decode_grid_size(dev);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D view [num_blocks * block_size tokens][num_kv_heads][head_dim] of one
+// cache, box = 64 dims x 1 head x 16 tokens, 128-byte swizzle.
+int encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int32_t block_size,
+                     int32_t hkv, int32_t d) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                        static_cast<cuuint64_t>(num_blocks * block_size)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(hkv)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(block_size)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return PKV_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_last_error(void) { return last_error_slot().c_str(); }
+
+int pkv_version(void) { return kVersion; }
+
+int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride,
+                          int64_t value_stride, void* key_cache, void* value_cache,
+                          const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                          int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t dtype, uint32_t* error_word, void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PKV_E_INVALID, "pkv_reshape_and_cache: sizes must be positive");
+  if (dtype != PKV_F32 && dtype != PKV_BF16)
+    return fail(PKV_E_UNSUPPORTED, "pkv_reshape_and_cache: dtype %d", dtype);
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+    return fail(PKV_E_INVALID, "pkv_reshape_and_cache: null pointer");
+  const int64_t esize = dtype == PKV_F32 ? 4 : 2;
+  const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * esize;
+  if (row_bytes % 16 || (key_stride * esize) % 16 || (value_stride * esize) % 16 ||
+      !aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_E_INVALID, "pkv_reshape_and_cache: rows, strides and bases must be 16-byte aligned");
+  if (key_stride < num_kv_heads * static_cast<int64_t>(head_dim) ||
+      value_stride < num_kv_heads * static_cast<int64_t>(head_dim))
+    return fail(PKV_E_INVALID, "pkv_reshape_and_cache: token stride shorter than a row");
+  cudaError_t e = launch_reshape_and_cache(key, value, key_stride * esize, value_stride * esize,
+                                           key_cache, value_cache, slot_mapping, num_tokens,
+                                           num_blocks * block_size, row_bytes, error_word,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "reshape_and_cache launch");
+}
+
+size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_t head_dim) {
+  if (num_reqs < 0 || num_heads <= 0 || head_dim <= 0) return 0;
+  return workspace_layout(num_reqs, num_heads, head_dim, current_grid()).total;
+}
+
+int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_cache,
+                               const void* value_cache, const int32_t* block_table,
+                               int32_t block_table_stride, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                               float scale, void* out, int64_t out_stride, int64_t num_tokens,
+                               int32_t num_reqs, int64_t num_blocks, int32_t block_size,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t dtype, int32_t max_query_len, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (num_tokens < 0 || num_reqs < 0 || num_blocks <= 0 || num_heads <= 0 || num_kv_heads <= 0)
+    return fail(PKV_E_INVALID, "pkv_paged_attention_varlen: bad sizes");
+  if (dtype != PKV_F32 && dtype != PKV_BF16)
+    return fail(PKV_E_UNSUPPORTED, "pkv_paged_attention_varlen: dtype %d", dtype);
+  if (block_size != 16) return fail(PKV_E_UNSUPPORTED, "block_size must be 16 (got %d)", block_size);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_E_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", head_dim);
+  if (num_heads % num_kv_heads) return fail(PKV_E_INVALID, "num_heads %% num_kv_heads != 0");
+  if (num_blocks * block_size > kMaxTmaRows)
+    return fail(PKV_E_UNSUPPORTED, "pool of %lld blocks is too large", static_cast<long long>(num_blocks));
+  if (!workspace) return fail(PKV_E_WORKSPACE, "workspace is required");
+  const int grid = current_grid();
+  const WorkspaceLayout wl = workspace_layout(num_reqs, num_heads, head_dim, grid);
+  if (workspace_bytes < wl.total)
+    return fail(PKV_E_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, wl.total);
+  if (num_tokens == 0 || num_reqs == 0) return PKV_OK;
+  if (!q || !key_cache || !value_cache || !block_table || !query_start_loc || !seq_lens ||
+      !num_computed_tokens || !out)
+    return fail(PKV_E_INVALID, "pkv_paged_attention_varlen: null pointer");
+  const int64_t row = static_cast<int64_t>(num_heads) * head_dim;
+  if (q_stride < row || out_stride < row || q_stride % 8 || out_stride % 8 || !aligned16(q) ||
+      !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_E_INVALID, "q/out/caches must be 16-byte aligned with strides >= heads*dim, multiple of 8");
+  if (block_table_stride <= 0) return fail(PKV_E_INVALID, "block_table_stride must be positive");
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AttnArgs a;
+  a.q = q;
+  a.q_stride = q_stride;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_table = block_table;
+  a.bt_stride = block_table_stride;
+  a.qsl = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.num_computed = num_computed_tokens;
+  a.out = out;
+  a.out_stride = out_stride;
+  a.num_tokens = num_tokens;
+  a.num_reqs = num_reqs;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  a.err = reinterpret_cast<uint32_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (dtype == PKV_F32) {
+    cudaError_t e = launch_attn_rows(a, false, false, st);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "attention launch");
+  }
+
+  // bf16: decode rows on the split-KV kernel, longer rows on the prefill path
+  if (num_kv_heads > 8 || num_heads / num_kv_heads > 16)
+    return fail(PKV_E_UNSUPPORTED, "bf16 path supports num_kv_heads <= 8 and G <= 16");
+  CUtensorMap kmap, vmap;
+  int rc = encode_cache_map(&kmap, key_cache, num_blocks, block_size, num_kv_heads, head_dim);
+  if (rc != PKV_OK) return rc;
+  rc = encode_cache_map(&vmap, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
+  if (rc != PKV_OK) return rc;
+  DecodeScratch ds;
+  ds.counters = reinterpret_cast<int32_t*>(ws + wl.counters);
+  ds.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
+  ds.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+  ds.num_slots = wl.slots;
+  cudaError_t e = launch_decode_bf16(a, kmap, vmap, ds, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (max_query_len != 1) {
+    e = launch_attn_rows(a, true, true, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

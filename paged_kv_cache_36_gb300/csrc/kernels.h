@@ -1,0 +1,61 @@
+// Launchers of the device kernels, called by the C ABI in api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace pkv {
+
+// Everything an attention kernel needs about one paged_attention_varlen call.
+struct AttnArgs {
+  const void* q;
+  int64_t q_stride;           // elements
+  const void* key_cache;
+  const void* value_cache;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* num_computed;
+  void* out;
+  int64_t out_stride;         // elements
+  int64_t num_tokens;
+  int32_t num_reqs;
+  int64_t num_blocks;
+  int32_t block_size;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  float scale;
+  uint32_t* err;              // device error word
+};
+
+// Scratch carved out of the caller's workspace for the split-KV decode.
+struct DecodeScratch {
+  int32_t* counters;          // [num_reqs], zero between calls
+  float* part_o;              // [slots][num_heads][head_dim]
+  float* part_ml;             // [slots][num_heads][2]: running max (log2 units), sum
+  int64_t num_slots;          // = decode grid size + num_reqs
+};
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t key_stride_b,
+                                     int64_t value_stride_b, void* key_cache, void* value_cache,
+                                     const int64_t* slot_mapping, int64_t num_tokens,
+                                     int64_t num_slots, int64_t row_bytes, uint32_t* err,
+                                     cudaStream_t stream);
+
+// Grid size (CTAs) of the persistent split-KV decode kernel on this device.
+int decode_grid_size(int device);
+
+// Split-KV decode of every request with query length 1 (bf16, mma + TMA).
+cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               const DecodeScratch& ws, int grid, cudaStream_t stream);
+
+// CUDA-core attention, one warp per (query row, head); fp32 path for all rows,
+// or only rows of requests with query length > 1 when skip_decode is set.
+cudaError_t launch_attn_rows(const AttnArgs& a, bool bf16, bool skip_decode, cudaStream_t stream);
+
+}  // namespace pkv

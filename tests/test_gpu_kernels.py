@@ -1,0 +1,231 @@
+"""GPU parity of reshape_and_cache and paged_attention_varlen against the oracle.
+
+Bit-exact cache images for reshape_and_cache; float tolerances for attention:
+max-abs <= 1e-5 in float32; max-abs <= 2e-2 and relative Frobenius error
+<= 1e-2 (overall and per request) in bfloat16.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import paging
+from tests.gpu_support import Batch, compare
+from workloads import configs
+from workloads.configs import KVHistory
+from workloads.generators import randn_fp32, random_block_placement, uniform_int
+
+pytestmark = pytest.mark.gpu
+
+
+def _pkv():
+    import paged_kv_cache_36_gb300 as pkv
+    return pkv
+
+
+def _sub_history(tensors_k, tensors_v):
+    lengths = np.array([k.shape[0] for k in tensors_k], np.int64)
+    offsets = np.concatenate([[0], np.cumsum(lengths)[:-1]]).astype(np.int64)
+    return KVHistory(torch.cat(tensors_k), torch.cat(tensors_v), lengths, offsets)
+
+
+# ---------------------------------------------------------------- reshape_and_cache
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("hkv,d", [(2, 64), (8, 128)])
+def test_reshape_and_cache_bit_exact(dtype, hkv, d):
+    pkv = _pkv()
+    NB, B, T = 64, 16, 300
+    g = torch.Generator().manual_seed(7)
+    key = torch.randn(T, hkv, d, generator=g).to(dtype)
+    value = torch.randn(T, hkv, d, generator=g).to(dtype)
+    slots = torch.randperm(NB * B, generator=g)[:T].to(torch.int64)
+    slots[::17] = -1                                          # padding tokens
+    kc_ref = torch.randn(NB, B, hkv, d, generator=g).to(dtype)
+    vc_ref = torch.randn(NB, B, hkv, d, generator=g).to(dtype)
+    kc, vc = kc_ref.cuda(), vc_ref.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.reshape_and_cache(key.cuda(), value.cuda(), kc, vc, slots.cuda(), error_word=err)
+    paging.write_cache(kc_ref, vc_ref, key, value, slots.tolist())
+    torch.cuda.synchronize()
+    assert torch.equal(kc.cpu().view(torch.int16 if dtype == torch.bfloat16 else torch.int32),
+                       kc_ref.view(torch.int16 if dtype == torch.bfloat16 else torch.int32))
+    assert torch.equal(vc.cpu(), vc_ref)
+    assert err.item() == 0
+
+
+def test_reshape_and_cache_strided_input_and_bad_slot():
+    pkv = _pkv()
+    NB, B, hkv, d, T = 8, 16, 2, 64, 40
+    qkv = torch.randn(T, 3 * hkv, d, dtype=torch.bfloat16)     # fused rows: K, V are strided views
+    key, value = qkv[:, hkv:2 * hkv], qkv[:, 2 * hkv:]
+    slots = torch.arange(T, dtype=torch.int64)
+    slots[5] = NB * B + 3                                       # past the pool: skipped and flagged
+    kc = torch.zeros(NB, B, hkv, d, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    kg, vg = kc.cuda(), vc.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qg = qkv.cuda()
+    pkv.reshape_and_cache(qg[:, hkv:2 * hkv], qg[:, 2 * hkv:], kg, vg, slots.cuda(), error_word=err)
+    good = [int(s) if i != 5 else -1 for i, s in enumerate(slots)]
+    paging.write_cache(kc, vc, key, value, good)
+    torch.cuda.synchronize()
+    assert torch.equal(kg.cpu(), kc) and torch.equal(vg.cpu(), vc)
+    assert err.item() & pkv.ERR_SLOT
+
+
+# ---------------------------------------------------------------- tiny config
+def _tiny_batch(case, reqs, query_len, num_computed, dtype):
+    """Batch over requests `reqs` of the tiny case (their own histories)."""
+    kv = _sub_history([case.kv.k(r) for r in reqs], [case.kv.v(r) for r in reqs])
+    q = torch.cat([case.q[r][nc:nc + ql] for r, nc, ql in zip(reqs, num_computed, query_len)])
+    blocks = [np.array(case.block_tables[r], np.int32) for r in reqs]
+    b = Batch(kv, blocks, case.num_blocks, query_len, num_computed, q, case.num_heads, dtype)
+    return b
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_tiny_decode_step(dtype):
+    case = configs.tiny_fp32_case(dtype)
+    # request 0: 40 tokens, query at position 39 (slot 199); request 1: 20 tokens, position 19 (slot 115)
+    b = _tiny_batch(case, [0, 1], [1, 1], [39, 19], dtype).alloc_cache().fill_history().upload_metadata()
+    assert b.slot_mapping.tolist() == [199, 115]
+    b.write_new_tokens()
+    out = b.attention()
+    compare(out, b.oracle(), b.qsl_host, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_tiny_chunked_prefill_equals_full(dtype):
+    case = configs.tiny_fp32_case(dtype)
+    pkv = _pkv()
+    shape = (case.num_blocks, 16, case.num_kv_heads, case.head_dim)
+    kc = torch.empty(shape, dtype=dtype, device="cuda")
+    vc = torch.empty_like(kc)
+    chunks = []
+    for a, e in [(0, 3), (3, 6), (6, 7)]:
+        b = _tiny_batch(case, [1], [e - a], [a], dtype)
+        b.key_cache, b.value_cache = kc, vc                # the cache carries over between chunks
+        b.upload_metadata()
+        assert b.slot_mapping.tolist() == list(range(48 + a, 48 + e))
+        b.write_new_tokens()
+        chunks.append(b.attention().clone())
+        compare(chunks[-1], b.oracle(), b.qsl_host, dtype)
+    full_b = _tiny_batch(case, [1], [7], [0], dtype).alloc_cache().upload_metadata().write_new_tokens()
+    full = full_b.attention()
+    chunked = torch.cat(chunks)
+    ref = full_b.oracle()
+    compare(chunked, ref, full_b.qsl_host, dtype)
+    compare(full, ref, full_b.qsl_host, dtype)
+    if dtype == torch.float32:
+        assert (chunked - full).abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_tiny_mixed_step(dtype):
+    case = configs.tiny_fp32_case(dtype)
+    # request 0 decodes at position 39 while request 1 runs chunk [3, 6)
+    b = _tiny_batch(case, [0, 1], [1, 3], [39, 3], dtype).alloc_cache().fill_history().upload_metadata()
+    assert b.slot_mapping.tolist() == [199, 51, 52, 53]
+    b.write_new_tokens()
+    compare(b.attention(), b.oracle(), b.qsl_host, dtype)
+
+
+# ---------------------------------------------------------------- random varlen batches
+CASES = [
+    # (H, Hkv, D, query lens, num_computed) - several tiles, ragged tails, empty requests
+    (32, 8, 128, [1, 1, 1, 1, 1, 1], [0, 15, 16, 17, 250, 1031]),
+    (32, 8, 128, [1, 37, 0, 1, 130, 1], [700, 0, 5, 3000, 300, 44]),
+    (8, 8, 64, [1, 5, 1, 64], [100, 30, 1, 0]),
+    (16, 2, 128, [1, 1, 2, 1], [513, 2, 77, 4095]),
+    (64, 8, 128, [1, 1, 9], [2000, 31, 100]),
+    (4, 1, 64, [1, 20, 1], [63, 16, 1000]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_random_varlen_bf16(case):
+    H, Hkv, D, qlens, ncs = CASES[case]
+    name = f"varlen{case}"
+    seq = [a + b for a, b in zip(qlens, ncs)]
+    counts = [max(1, (s + 15) // 16) for s in seq]
+    NB = 4 * sum(counts) + 8
+    blocks = random_block_placement(NB, counts, name, "placement")
+    lengths = np.array(seq, np.int64)
+    offsets = np.concatenate([[0], np.cumsum(lengths)[:-1]]).astype(np.int64)
+    n = int(lengths.sum())
+    kv = KVHistory(randn_fp32((n, Hkv, D), name, "k", dtype=torch.bfloat16),
+                   randn_fp32((n, Hkv, D), name, "v", dtype=torch.bfloat16), lengths, offsets)
+    q = randn_fp32((sum(qlens), H, D), name, "q", dtype=torch.bfloat16)
+    b = Batch(kv, blocks, NB, qlens, ncs, q, H, torch.bfloat16).alloc_cache().fill_history()
+    b.upload_metadata().write_new_tokens()
+    compare(b.attention(), b.oracle(), b.qsl_host, torch.bfloat16)
+
+
+def test_workspace_reuse_and_error_word():
+    pkv = _pkv()
+    H, Hkv, D = 32, 8, 128
+    name = "reuse"
+    ctx = [3000, 200, 4096, 17]
+    counts = [(c + 15) // 16 for c in ctx]
+    NB = sum(counts) + 4
+    blocks = random_block_placement(NB, counts, name, "placement")
+    lengths = np.array(ctx, np.int64)
+    offsets = np.concatenate([[0], np.cumsum(lengths)[:-1]]).astype(np.int64)
+    kv = KVHistory(randn_fp32((int(lengths.sum()), Hkv, D), name, "k", dtype=torch.bfloat16),
+                   randn_fp32((int(lengths.sum()), Hkv, D), name, "v", dtype=torch.bfloat16),
+                   lengths, offsets)
+    q = randn_fp32((4, H, D), name, "q", dtype=torch.bfloat16)
+    b = Batch(kv, blocks, NB, [1] * 4, [c - 1 for c in ctx], q, H, torch.bfloat16)
+    b.alloc_cache().fill_history().upload_metadata().write_new_tokens()
+    ws = pkv.new_workspace(64, H, D)
+    first = b.attention(workspace=ws).clone()
+    second = b.attention(workspace=ws).clone()
+    assert torch.equal(first, second)                 # split counters were left at zero
+    compare(first, b.oracle(), b.qsl_host, torch.bfloat16)
+    assert pkv.read_error_word(ws) == 0
+    # an out-of-range block id is reported, not faulted on (TMA reads zeros there)
+    bad = b.block_table.clone()
+    bad[1, 0] = NB + 5
+    pkv.paged_attention_varlen(b.q, b.key_cache, b.value_cache, bad, b.qsl, b.seq_lens, b.nc,
+                               1 / math.sqrt(D), workspace=ws, max_query_len=1)
+    assert pkv.read_error_word(ws) & pkv.ERR_BLOCK_ID
+    ws.zero_()
+    third = b.attention(workspace=ws)
+    assert torch.equal(first, third)
+
+
+# ---------------------------------------------------------------- full-size configs
+def _decode_cfg_batch(cfg):
+    return Batch(cfg.kv, cfg.blocks, cfg.num_blocks, np.ones(len(cfg.context), np.int64),
+                 cfg.context - 1, cfg.q, cfg.num_heads, cfg.dtype)
+
+
+def test_config2_decode_llama8b():
+    cfg = configs.decode_batch_llama8b()
+    b = _decode_cfg_batch(cfg).alloc_cache().fill_history().upload_metadata().write_new_tokens()
+    out = b.attention()
+    compare(out, b.oracle(), b.qsl_host, torch.bfloat16)
+
+
+def test_config3_mixed_chunked_step():
+    cfg = configs.mixed_chunked_step()
+    b = Batch(cfg.kv, cfg.blocks, cfg.num_blocks, cfg.query_len, cfg.num_computed, cfg.q,
+              cfg.num_heads, cfg.dtype).alloc_cache().fill_history().upload_metadata()
+    b.write_new_tokens()
+    # this step's 768 new tokens landed bit-exactly at their slots
+    _, _, slots = b.new_tokens()
+    got = b.key_cache.view(-1, b.Hkv, b.D)[torch.tensor(slots, device="cuda")]
+    assert torch.equal(got, b.k_new)
+    out = b.attention()
+    compare(out, b.oracle(), b.qsl_host, torch.bfloat16)
+
+
+@pytest.mark.slow
+def test_config4_long_decode_llama70b():
+    cfg = configs.long_decode_llama70b()
+    b = _decode_cfg_batch(cfg).alloc_cache().fill_history().upload_metadata().write_new_tokens()
+    out = b.attention()
+    compare(out, b.oracle(), b.qsl_host, torch.bfloat16)

@@ -1,0 +1,166 @@
+"""The C++ host path (allocator, scheduler, metadata builder) against the
+oracle's independent list-based implementations, compared bit-exactly after
+every transition.  CPU only."""
+
+import random
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_36_gb300 as pkv
+from oracle import paging
+from oracle.allocator import NaiveAllocator
+from oracle.scheduler import NaiveScheduler, SchedConfig
+from workloads import generate_arrivals, trace_spec
+
+
+def _same_alloc(cpp: pkv.Allocator, ref: NaiveAllocator, ids):
+    assert cpp.free_list() == ref.free_list
+    for r in ids:
+        assert cpp.table(r) == ref.table(r)
+        assert cpp.held_tokens(r) == ref.held_tokens(r)
+    s, t = cpp.stats(), ref.stats()
+    assert (s["capacity"], s["free"], s["reserved"], s["committed"], s["num_requests"],
+            s["tail_waste"], s["alloc_failures"], s["peak_used"]) == \
+        (t.capacity, t.free, t.reserved, t.committed, t.num_requests, t.tail_waste,
+         t.alloc_failures, t.peak_used)
+    cpp.check()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_allocator_random_ops(seed):
+    rng = random.Random(seed)
+    B = rng.choice([1, 4, 16])
+    nb = rng.choice([8, 33, 100])
+    cpp, ref = pkv.Allocator(nb, B, 64), NaiveAllocator(nb, B, 64)
+    ids = list(range(10))
+    for _ in range(600):
+        op = rng.random()
+        if op < 0.5:
+            plan = [(r, rng.randint(0, 3 * B)) for r in rng.sample(ids, rng.randint(1, 4))]
+            a, b = cpp.reserve(plan), ref.reserve(plan)
+            assert a == b
+            if a:
+                if rng.random() < 0.3:      # cancel one planned request mid-step
+                    r = rng.choice(plan)[0]
+                    assert cpp.free_request(r) == ref.free_request(r)
+                if rng.random() < 0.75:
+                    cpp.commit(); ref.commit()
+                else:
+                    cpp.rollback(); ref.rollback()
+        else:
+            r = rng.choice(ids)
+            assert cpp.free_request(r) == ref.free_request(r)
+        _same_alloc(cpp, ref, ids)
+
+
+def test_allocator_state_errors():
+    a = pkv.Allocator(4, 4, 16)
+    with pytest.raises(pkv.PkvError):
+        a.commit()
+    assert a.reserve([(0, 4)])
+    with pytest.raises(pkv.PkvError):
+        a.reserve([(1, 1)])
+    a.rollback()
+    with pytest.raises(pkv.PkvError):
+        a.reserve([(0, 1), (0, 1)])
+    assert not a.reserve([(0, 17)])          # 5 blocks from a pool of 4
+    assert a.stats()["alloc_failures"] == 1
+    b = pkv.Allocator(8, 4, 2)
+    with pytest.raises(pkv.PkvError):
+        b.reserve([(0, 9)])                  # 3 blocks > the 2-entry row
+
+
+def test_slot_mapping_builder():
+    # the worked example: [5, 8, 12], block_size 16, position 25 -> 137
+    out = pkv.build_slot_mapping(np.array([[5, 8, 12]]), [0, 1], [25], 16)
+    assert out.tolist() == [137]
+    rng = random.Random(3)
+    for _ in range(50):
+        R = rng.randint(1, 6)
+        B = rng.choice([1, 4, 16])
+        qlens = [rng.randint(0, 9) for _ in range(R)]
+        ncs = [rng.randint(0, 40) for _ in range(R)]
+        width = max((nc + ql + B - 1) // B for nc, ql in zip(ncs, qlens)) + 1
+        rows = [rng.sample(range(500), width) for _ in range(R)]
+        qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+        got = pkv.build_slot_mapping(np.array(rows, np.int32), qsl, ncs, B)
+        assert got.tolist() == paging.slot_mapping(rows, qlens, ncs, B)
+    with pytest.raises(pkv.PkvError):
+        pkv.build_slot_mapping(np.array([[1]]), [0, 1], [16], 16)   # position past the row
+
+
+def _pair(c: SchedConfig):
+    ref = NaiveScheduler(c, deep_checks=False)
+    cpp = pkv.Scheduler(c.max_num_seqs, c.max_num_batched_tokens, c.chunk_size, c.max_model_len,
+                        c.block_size, c.num_blocks, c.max_blocks_per_req,
+                        c.artificial_preempt_prob, c.artificial_preempt_max, c.artificial_seed)
+    return cpp, ref
+
+
+def _compare_step(cpp, ref, arrivals_now, fail_step=False, check_tables=True):
+    for a in arrivals_now:
+        assert cpp.add_request(a.req_id, a.prompt_len, a.max_output) == \
+            ref.add_request(a.req_id, a.prompt_len, a.max_output)
+    pc = cpp.step()
+    pr = ref.step()
+    assert pc["entries"] == pr.entries
+    assert pc["preempted"] == pr.preempted
+    assert pc["admitted"] == pr.admitted
+    bt, qsl, seq, nc, slots = cpp.metadata()
+    rqsl, rseq, rnc, rrows, rslots = ref.metadata(pr)
+    assert qsl.tolist() == rqsl and seq.tolist() == rseq and nc.tolist() == rnc
+    assert slots.tolist() == rslots
+    for k, row in enumerate(rrows):
+        assert bt[k, :len(row)].tolist() == row and (bt[k, len(row):] == -1).all()
+    if check_tables:
+        assert cpp.allocator.free_list() == ref.alloc.free_list
+    fin_c = cpp.finish_step(not fail_step)
+    fin_r = ref.finish_step(not fail_step)
+    assert fin_c == fin_r
+    run, wait = cpp.queues()
+    assert run == ref.running and wait == ref.waiting
+    return pc
+
+
+def test_scheduler_trace_bit_exact():
+    spec = trace_spec()
+    c = SchedConfig(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                    spec.max_model_len, spec.block_size, spec.num_blocks,
+                    spec.max_model_len // spec.block_size)
+    cpp, ref = _pair(c)
+    by_step = {}
+    for a in generate_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    for step in range(spec.steps):
+        _compare_step(cpp, ref, by_step.get(step, []), check_tables=(step % 10 == 0))
+        if step % 25 == 0:
+            cpp.allocator.check()
+            for rid, r in ref.reqs.items():
+                st = cpp.request(rid)
+                assert (st["num_tokens"], st["num_computed"], st["outputs"], st["preemptions"]) == \
+                    (r.num_tokens, r.num_computed, r.outputs, r.preemptions)
+    cnt = cpp.counters()
+    assert cnt["preemptions"] == ref.total_preemptions > 0
+    assert cnt["recomputed_tokens"] == ref.recomputed_tokens
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_scheduler_small_random_with_faults(seed):
+    rng = random.Random(seed)
+    c = SchedConfig(max_num_seqs=rng.choice([2, 4, 8]), max_num_batched_tokens=rng.choice([8, 20, 64]),
+                    chunk_size=rng.choice([3, 8, 16]), max_model_len=200, block_size=4,
+                    num_blocks=rng.choice([12, 24]), max_blocks_per_req=50,
+                    artificial_preempt_prob=0.5, artificial_preempt_max=rng.choice([0, 5, 500]),
+                    artificial_seed=seed)
+    cpp, ref = _pair(c)
+    rid = 0
+    for step in range(200):
+        arrivals = []
+        for _ in range(rng.choice([0, 0, 1, 2])):
+            arrivals.append(type("A", (), {"req_id": rid, "prompt_len": rng.randint(1, 30),
+                                           "max_output": rng.randint(1, 12)})())
+            rid += 1
+        _compare_step(cpp, ref, arrivals, fail_step=rng.random() < 0.1)
+        cpp.allocator.check()
+    assert cpp.counters()["inject_left"] == ref.inject_left

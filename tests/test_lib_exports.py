@@ -1,0 +1,65 @@
+"""The C-ABI library loads and exports every entry point include/pkv.h declares
+(no GPU needed: nothing here launches a kernel)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def declared_symbols():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(pkv_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def libpkv():
+    from paged_kv_cache_36_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for must in ["pkv_reshape_and_cache", "pkv_paged_attention_varlen",
+                 "pkv_attention_workspace_bytes", "pkv_alloc_reserve", "pkv_alloc_commit",
+                 "pkv_alloc_rollback", "pkv_sched_step", "pkv_build_slot_mapping"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(libpkv):
+    missing = [n for n in declared_symbols() if not hasattr(libpkv, n)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_header():
+    from paged_kv_cache_36_gb300 import _ffi
+    assert set(declared_symbols()) <= set(_ffi.SIGNATURES)
+
+
+def test_version_and_error_string(libpkv):
+    import paged_kv_cache_36_gb300 as pkv
+    assert pkv.lib().pkv_version() >= 1
+    # a host-side error sets the thread-local message
+    assert pkv.lib().pkv_alloc_commit(None) == -1
+    assert b"null handle" in pkv.lib().pkv_last_error()
+
+
+def test_bad_arguments_rejected_without_gpu(libpkv):
+    import paged_kv_cache_36_gb300 as pkv
+    L = pkv.lib()
+    # block_size other than 16 is refused before any CUDA call
+    rc = L.pkv_paged_attention_varlen(None, 0, None, None, None, 0, None, None, None, 1.0, None,
+                                      0, 1, 1, 16, 8, 4, 2, 64, 1, 0, None, 0, None)
+    assert rc == -2
+    rc = L.pkv_reshape_and_cache(None, None, 0, 0, None, None, None, 1, 16, 16, 2, 64, 7, None, None)
+    assert rc == -2
