@@ -130,6 +130,35 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
                                size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_attention_varlen without a workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory
+ * where they run attention - an engine plugin whose enqueue step must not
+ * allocate, a server that gave all free HBM to the KV block pool up front, or
+ * a latency-critical loop that must avoid what cudaMalloc/cudaFree can cost.
+ *
+ * Same arguments and result as pkv_paged_attention_varlen, minus the
+ * workspace.  The split-KV scratch lives in a 16 MiB array compiled into the
+ * library (held by every GPU that loads it until the process exits); a batch
+ * whose scratch (pkv_attention_workspace_bytes) exceeds 16 MiB is rejected
+ * with PKV_E_WORKSPACE.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current): make that
+ * first call before any stream capture begins.  Every call clears the
+ * scratch's error word and split counters on `stream` before its kernels and
+ * calls no allocating routine.  All calls share the array, so calls whose
+ * work overlaps on the GPU race: serialise them.  error_word (device uint32,
+ * or NULL) receives this call's PKV_ERR_* bits.
+ * ---------------------------------------------------------------------- */
+int pkv_paged_attention_varlen_noalloc(const void* q, int64_t q_stride, const void* key_cache,
+                                       const void* value_cache, const int32_t* block_table,
+                                       int32_t block_table_stride, const int32_t* query_start_loc,
+                                       const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                                       float scale, void* out, int64_t out_stride,
+                                       int64_t num_tokens, int32_t num_reqs, int64_t num_blocks,
+                                       int32_t block_size, int32_t num_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                                       int32_t max_query_len, uint32_t* error_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * Step metadata (host)  [AI Infra, section "Paged Attention": slot_idx =
  * block_table[r][pos // block_size] * block_size + pos % block_size]
  *

@@ -56,6 +56,9 @@ SIGNATURES = {
     "pkv_paged_attention_varlen": (C.c_int, [vp, i64, vp, vp, vp, i32, vp, vp, vp, f32, vp, i64,
                                              i64, i32, i64, i32, i32, i32, i32, i32, i32, vp, sz,
                                              vp]),
+    "pkv_paged_attention_varlen_noalloc": (C.c_int, [vp, i64, vp, vp, vp, i32, vp, vp, vp, f32,
+                                                     vp, i64, i64, i32, i64, i32, i32, i32, i32,
+                                                     i32, i32, vp, vp]),
     "pkv_build_slot_mapping": (C.c_int, [vp, i32, vp, vp, i32, i32, vp, i64]),
     "pkv_alloc_create": (vp, [i32, i32, i32]),
     "pkv_alloc_destroy": (None, [vp]),
