@@ -75,6 +75,25 @@ int encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int
   return PKV_OK;
 }
 
+// The [T, H, D] query (token stride q_stride elements) as a 3-D tensor
+// (D, H, T), box = 64 dims x G heads x 128/G tokens, 128-byte swizzle: one box
+// is the 128-row (token, head-in-group) tile of the prefill kernel.
+int encode_query_map(CUtensorMap* map, const void* q, int64_t q_stride, int64_t num_tokens,
+                     int32_t num_heads, int32_t group, int32_t d) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(num_heads),
+                        static_cast<cuuint64_t>(num_tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(q_stride) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled (query) failed (%d)", int(r));
+  return PKV_OK;
+}
+
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(PKV_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -186,8 +205,9 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
   }
 
   // bf16: decode rows on the split-KV kernel, longer rows on the prefill path
-  if (num_kv_heads > 8 || num_heads / num_kv_heads > 16)
-    return fail(PKV_E_UNSUPPORTED, "bf16 path supports num_kv_heads <= 8 and G <= 16");
+  const int group = num_heads / num_kv_heads;
+  if (num_kv_heads > 8 || group > 16 || (group & (group - 1)))
+    return fail(PKV_E_UNSUPPORTED, "bf16 path supports num_kv_heads <= 8 and G in {1,2,4,8,16}");
   CUtensorMap kmap, vmap;
   int rc = encode_cache_map(&kmap, key_cache, num_blocks, block_size, num_kv_heads, head_dim);
   if (rc != PKV_OK) return rc;
@@ -201,7 +221,11 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
   cudaError_t e = launch_decode_bf16(a, kmap, vmap, ds, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (max_query_len != 1) {
-    e = launch_attn_rows(a, true, true, st);
+    CUtensorMap qmap;
+    rc = encode_query_map(&qmap, q, q_stride, num_tokens, num_heads, num_heads / num_kv_heads,
+                          head_dim);
+    if (rc != PKV_OK) return rc;
+    e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   return PKV_OK;

@@ -54,6 +54,12 @@ int decode_grid_size(int device);
 cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const DecodeScratch& ws, int grid, cudaStream_t stream);
 
+// Chunked-prefill attention (bf16, tcgen05 + TMA + TMEM) of every request
+// with query length > 1; qmap is the [T, H, D] query as a (D, H, T) tensor map
+// with a 64 x G x 128/G box.
+cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, int grid, cudaStream_t stream);
+
 // CUDA-core attention, one warp per (query row, head); fp32 path for all rows,
 // or only rows of requests with query length > 1 when skip_decode is set.
 cudaError_t launch_attn_rows(const AttnArgs& a, bool bf16, bool skip_decode, cudaStream_t stream);
