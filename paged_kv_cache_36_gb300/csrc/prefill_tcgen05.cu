@@ -12,23 +12,27 @@
 // tiles of 128 = eight 16-token paged blocks; each block is one TMA box per
 // 64-dim half, landing 128-byte swizzled so that the 8 boxes form one
 // [128 keys x 64 dims] operand region.  Per key tile j:
-//   S_j = Q K_j^T   (tcgen05.mma M=128 N=128 K=D, fp32 in tensor memory)
-//   softmax rows   (one thread per row: tcgen05.ld of its S row, causal mask,
-//                   running max, exp2, P as bf16 into a swizzled smem tile)
-//   O  += P_j V_j  (tcgen05.mma M=128 N=D K=128, V read MN-major)
-// S is double-buffered in tensor memory, so S_{j+1} is computed while the
-// softmax of tile j runs.  The running max is only moved (and O, l rescaled)
-// when a row's new max exceeds the one in use by more than 2^8; otherwise the
-// stale max keeps P <= 256, which is exact arithmetic with a different
-// reference point.
+//   S_j = Q K_j^T   tcgen05.mma M=128 N=128 K=D, both operands in shared
+//                   memory, fp32 result in tensor memory (double-buffered)
+//   softmax        one thread per row reads its S row from tensor memory,
+//                   applies the causal mask on absolute positions, updates the
+//                   running max and sum, and writes P (bf16) back into tensor
+//                   memory (double-buffered)
+//   O  += P_j V_j  tcgen05.mma with A = P from tensor memory, B = V read
+//                   MN-major from shared memory, O in tensor memory
+// With S and P both double-buffered, QK^T of tile j+1 and PV of tile j-1 run
+// on the tensor core while the softmax of tile j runs.  A row's running max is
+// only moved (and its O, l rescaled) when the new max exceeds the one in use
+// by more than 2^8; otherwise the stale max keeps P <= 256, which is the same
+// arithmetic with a different reference point.
 //
-// Warp roles (6 warps): warp 0 issues TMA (Q once per tile, K/V through a
-// 2-stage ring), warp 1 owns the tensor memory and issues MMAs from one
-// thread, warps 2-5 (one per 32-lane quadrant of tensor memory) run the
-// softmax and the epilogue.  Tiles are handed out persistently by a
-// device-side plan over query_start_loc, so no host copy of the metadata is
-// needed.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and an abort
-// flag that stops all roles.
+// Warp roles (6 warps): warp 0 issues TMA (Q once per tile, K through a
+// 3-stage ring, V through a 2-stage ring), warp 1 owns the tensor memory and
+// issues MMAs from one thread, warps 2-5 (one per 32-lane quadrant of tensor
+// memory) run the softmax and the epilogue.  Tiles are handed out
+// persistently by a device-side plan over query_start_loc.  Every wait is
+// bounded; a timeout sets PKV_ERR_TIMEOUT and an abort flag that stops all
+// roles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,12 +50,23 @@ constexpr int kRows = 128;
 constexpr int kKeys = 128;
 constexpr uint32_t kRegion = 16384;  // 128 rows x 128 bytes
 constexpr uint32_t kBox = 2048;      // 16 rows x 128 bytes
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256, 256 + D)
-constexpr uint32_t kColO = 256;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+// tensor memory columns: S0, S1 (fp32 128 each), P0, P1 (bf16 pairs, 64 each), O
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColP = 256;
+constexpr uint32_t kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-enum Bar { kQFull, kQEmpty, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull0, kSFull1,
-           kSFree0, kSFree1, kPFull, kODone, kNumBars };
+enum Bar {
+  kQFull, kQEmpty,
+  kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2,
+  kVFull0, kVFull1, kVEmpty0, kVEmpty1,
+  kSFull0, kSFull1, kSFree0, kSFree1,
+  kPFull0, kPFull1, kODone0, kODone1,
+  kNumBars
+};
 
 struct PrefillParams {
   const int32_t* block_table;
@@ -71,6 +86,7 @@ struct PrefillParams {
 
 struct Tile {
   int r, h, u0, ntok, nkeys, nkt;
+  int first;  // key tile processed first (see key_tile)
   int64_t qs;
   int nc;
 };
@@ -78,13 +94,11 @@ struct Tile {
 template <int D>
 struct Layout {
   static constexpr int NDH = D / 64;
+  static constexpr uint32_t kHalf = NDH * kRegion;  // one K (or V) tile
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kQBytes = NDH * kRegion;
-  static constexpr uint32_t kKV = kQBytes;
-  static constexpr uint32_t kKVHalf = NDH * kRegion;      // K (or V) of one stage
-  static constexpr uint32_t kKVStage = 2 * kKVHalf;
-  static constexpr uint32_t kP = kKV + 2 * kKVStage;
-  static constexpr uint32_t kBars = kP + 2 * kRegion;
+  static constexpr uint32_t kK = kQ + kHalf;
+  static constexpr uint32_t kV = kK + kKStages * kHalf;
+  static constexpr uint32_t kBars = kV + kVStages * kHalf;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;  // tmem slot, abort flag
   static constexpr uint32_t kPrefix = kMisc + 16;
 };
@@ -108,7 +122,24 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int32_t* prefix, int
   t.ntok = min(tpt, qlen - t.u0);
   t.nkeys = t.nc + t.u0 + t.ntok;  // keys up to the last row's position
   t.nkt = (t.nkeys + kKeys - 1) / kKeys;
+  // CTAs sharing a KV head start at different key tiles so they do not all
+  // read the same cache lines at once; the first tile must be visible to every
+  // row (key0 <= smallest position), so the first row max is finite.
+  t.first = qt % ((t.nc + t.u0) / kKeys + 1);
   return t;
+}
+
+// Key tile handled at step j of a tile: a rotation of 0..nkt-1 (the online
+// softmax does not depend on the order in which keys arrive).
+__device__ __forceinline__ int key_tile(const Tile& t, int j) {
+  const int k = t.first + j;
+  return k < t.nkt ? k : k - t.nkt;
+}
+
+// All lanes of the calling warp wait; the result is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, err, abort));
 }
 
 }  // namespace
@@ -135,8 +166,8 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < kNumBars; ++b) {
-      const uint32_t cnt = (b == kSFree0 || b == kSFree1 || b == kPFull) ? 4u : 1u;
-      mbar_init(&bars[b], cnt);
+      const bool softmax_arrives = b == kSFree0 || b == kSFree1 || b == kPFull0 || b == kPFull1;
+      mbar_init(&bars[b], softmax_arrives ? 4u : 1u);
     }
     fence_mbar_init();
     *abort_flag = 0;
@@ -174,127 +205,133 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ============================ TMA producer ============================
-    uint32_t q_uses = 0, kv_count = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = decode_tile(tile, prefix, R, p, tpt);
-      int qok = 1;
-      if (lane == 0) {
-        if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag)) {
-          qok = 0;
-        } else {
-          mbar_arrive_expect_tx(&bars[kQFull], L::kQBytes);
+    // ============================ TMA producers ============================
+    // lane 0 streams Q and K, lane 1 streams V; each runs its own loop (no
+    // warp-collective operations), so K can run ahead while V waits for PV.
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      const int nst = is_k ? kKStages : kVStages;
+      const int full0 = is_k ? kKFull0 : kVFull0;
+      const int empty0 = is_k ? kKEmpty0 : kVEmpty0;
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      uint8_t* ring = smem + (is_k ? L::kK : L::kV);
+      uint32_t q_uses = 0, count = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, prefix, R, p, tpt);
+        if (is_k) {
+          if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag))
+            break;
+          mbar_arrive_expect_tx(&bars[kQFull], L::kHalf);
           for (int dh = 0; dh < NDH; ++dh)
             tma_load_3d(smem + L::kQ + dh * kRegion, &qmap, dh * 64, t.h * G,
                         static_cast<int32_t>(t.qs + t.u0), &bars[kQFull]);
+          ++q_uses;
         }
-      }
-      if (!__shfl_sync(0xffffffffu, qok, 0)) break;
-      ++q_uses;
-      const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
-      const int nblk = (t.nkeys + 15) / 16;
-      for (int j = 0; j < t.nkt; ++j) {
-        const int b0 = j * 8;
-        const int nvalid = min(8, nblk - b0);
-        int32_t phys = 0;
-        if (lane < nvalid) {
-          phys = __ldg(row + b0 + lane);
-          if (phys < 0 || phys >= p.num_blocks) {
-            atomicOr(p.err, PKV_ERR_BLOCK_ID);
-            phys = p.num_blocks;  // out of the tensor: TMA fills zeros
-          }
-        }
-        const int s = kv_count & 1;
-        const uint32_t n = kv_count >> 1;
-        int ok = 1;
-        if (lane == 0) {
-          if (n > 0 && !mbar_wait_or_abort(&bars[kKvEmpty0 + s], (n - 1) & 1, p.err, abort_flag)) {
-            ok = 0;
-          } else {
-            mbar_arrive_expect_tx(&bars[kKvFull0 + s], 2u * NDH * kBox * nvalid);
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        uint8_t* kst = smem + L::kKV + s * L::kKVStage;
-        uint8_t* vst = kst + L::kKVHalf;
-        for (int k = 0; k < nvalid; ++k) {
-          const int32_t pb = __shfl_sync(0xffffffffu, phys, k);
-          if (lane == 0) {
-            for (int dh = 0; dh < NDH; ++dh) {
-              tma_load_3d(kst + dh * kRegion + k * kBox, &kmap, dh * 64, t.h, pb * 16,
-                          &bars[kKvFull0 + s]);
-              tma_load_3d(vst + dh * kRegion + k * kBox, &vmap, dh * 64, t.h, pb * 16,
-                          &bars[kKvFull0 + s]);
+        const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
+        const int nblk = (t.nkeys + 15) / 16;
+        bool ok = true;
+        for (int j = 0; j < t.nkt && ok; ++j) {
+          const int b0 = key_tile(t, j) * 8;
+          const int nvalid = min(8, nblk - b0);
+          int32_t phys[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            int32_t v = k < nvalid ? __ldg(row + b0 + k) : 0;
+            if (k < nvalid && (v < 0 || v >= p.num_blocks)) {
+              if (is_k) atomicOr(p.err, PKV_ERR_BLOCK_ID);
+              v = p.num_blocks;  // out of the tensor: TMA fills zeros
             }
+            phys[k] = v;
           }
+          const int st = count % nst;
+          const uint32_t n = count / nst;
+          if (n > 0 && !mbar_wait_or_abort(&bars[empty0 + st], (n - 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars[full0 + st], NDH * kBox * nvalid);
+          uint8_t* dst = ring + st * L::kHalf;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (k < nvalid)
+              for (int dh = 0; dh < NDH; ++dh)
+                tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
+                            &bars[full0 + st]);
+          ++count;
         }
-        ++kv_count;
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
-    constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
-    uint32_t q_count = 0, kv_count = 0, s_count = 0, p_count = 0;
-    const uint32_t q_base = smem_u32(smem + L::kQ);
-    const uint32_t p_base = smem_u32(smem + L::kP);
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = decode_tile(tile, prefix, R, p, tpt);
+    // One thread issues S_j = Q K_j^T and O += P_j V_j in whatever order their
+    // inputs become ready (QK may run up to two tiles ahead of PV).
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
+      uint32_t q_count = 0, k_count = 0, v_count = 0, s_count = 0, pv = 0;
+      const uint32_t q_base = smem_u32(smem + L::kQ);
       bool ok = true;
-      if (lane == 0) ok = mbar_wait_or_abort(&bars[kQFull], q_count & 1, p.err, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      ++q_count;
-      int s_prev = 0;
-      for (int j = 0; j <= t.nkt && ok; ++j) {
-        if (j < t.nkt) {
-          // ---- S_j = Q K_j^T ----
-          const int s = kv_count & 1;
-          const int b = s_count & 1;
-          if (lane == 0) {
-            ok = mbar_wait_or_abort(&bars[kKvFull0 + s], (kv_count >> 1) & 1, p.err, abort_flag);
-            if (ok && (s_count >> 1) > 0)
-              ok = mbar_wait_or_abort(&bars[kSFree0 + b], ((s_count >> 1) - 1) & 1, p.err,
-                                      abort_flag);
-            if (ok) {
+      for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, prefix, R, p, tpt);
+        ok = mbar_wait_or_abort(&bars[kQFull], q_count & 1, p.err, abort_flag);
+        ++q_count;
+        int jq = 0, jp = 0;  // next QK, next PV of this tile
+        long long t0 = clock64();
+        while (ok && jp < t.nkt) {
+          bool progressed = false;
+          if (jq < t.nkt && jq < jp + 2) {
+            const int ks = k_count % kKStages;
+            const int b = s_count & 1;
+            if (mbar_try_wait(&bars[kKFull0 + ks], (k_count / kKStages) & 1) &&
+                ((s_count >> 1) == 0 || mbar_try_wait(&bars[kSFree0 + b], ((s_count >> 1) - 1) & 1))) {
               tc_fence_after();
-              const uint32_t k_base = smem_u32(smem + L::kKV + s * L::kKVStage);
+              const uint32_t k_base = smem_u32(smem + L::kK + ks * L::kHalf);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-                tc_mma_ss(tmem + b * kKeys, smem_desc_sw128(q_base + off, 16, 1024),
+                tc_mma_ss(tmem + kColS + b * kKeys, smem_desc_sw128(q_base + off, 16, 1024),
                           smem_desc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0);
               }
               tc_commit(&bars[kSFull0 + b]);
+              tc_commit(&bars[kKEmpty0 + ks]);
+              ++k_count;
+              ++s_count;
+              ++jq;
+              progressed = true;
             }
           }
-        }
-        if (j > 0 && ok && lane == 0) {
-          // ---- O += P_{j-1} V_{j-1} ----
-          ok = mbar_wait_or_abort(&bars[kPFull], p_count & 1, p.err, abort_flag);
-          if (ok) {
-            tc_fence_after();
-            const uint32_t v_base = smem_u32(smem + L::kKV + s_prev * L::kKVStage + L::kKVHalf);
+          if (jp < jq) {
+            const int pb = pv & 1;
+            const int vs = v_count % kVStages;
+            if (mbar_try_wait(&bars[kPFull0 + pb], (pv >> 1) & 1) &&
+                mbar_try_wait(&bars[kVFull0 + vs], (v_count / kVStages) & 1)) {
+              tc_fence_after();
+              const uint32_t v_base = smem_u32(smem + L::kV + vs * L::kHalf);
 #pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint32_t a_off = (kk >> 2) * kRegion + (kk & 3) * 32;
-              tc_mma_ss(tmem + kColO, smem_desc_sw128(p_base + a_off, 16, 1024),
-                        smem_desc_sw128(v_base + kk * 16 * 128, kRegion, 1024), idesc_o,
-                        (j > 1 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kKeys / 16; ++kk)
+                tc_mma_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8,
+                          smem_desc_sw128(v_base + kk * 16 * 128, kRegion, 1024), idesc_o,
+                          (jp > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(&bars[kODone0 + pb]);
+              tc_commit(&bars[kVEmpty0 + vs]);
+              ++v_count;
+              ++pv;
+              ++jp;
+              if (jp == t.nkt) tc_commit(&bars[kQEmpty]);
+              progressed = true;
             }
-            tc_commit(&bars[kODone]);
-            tc_commit(&bars[kKvEmpty0 + s_prev]);
-            if (j == t.nkt) tc_commit(&bars[kQEmpty]);
+          }
+          if (progressed) {
+            t0 = clock64();
+          } else if (*abort_flag) {
+            ok = false;
+          } else if (clock64() - t0 > kWaitLimitCycles) {
+            atomicOr(p.err, PKV_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
           }
         }
-        if (j > 0) ++p_count;
-        if (j < t.nkt) {
-          s_prev = kv_count & 1;
-          ++kv_count;
-          ++s_count;
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
     }
   } else {
@@ -302,53 +339,60 @@ __global__ void __launch_bounds__(192, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // tile row = tensor-memory lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    uint8_t* p_tile = smem + L::kP;
-    uint32_t s_count = 0, kv_count = 0, o_count = 0;
+    const float sl2 = p.scale_log2;
+    uint32_t s_count = 0, v_count = 0, pv = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Tile t = decode_tile(tile, prefix, R, p, tpt);
-      const int u = t.u0 + row / G;                   // token of this row within the request
-      const bool valid_row = (row / G) < t.ntok && row < tpt * G;
+      const int u = t.u0 + row / G;  // token of this row within the request
+      const bool valid_row = (row / G) < t.ntok;
       const int pos = t.nc + (valid_row ? u : t.u0 + t.ntok - 1);
+      const int pos_min = t.nc + t.u0;  // smallest position in the tile
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < t.nkt && ok; ++j) {
         const int b = s_count & 1;
-        const int s = kv_count & 1;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_or_abort(&bars[kSFull0 + b], (s_count >> 1) & 1, p.err, abort_flag));
-        if (!ok) break;
+        const int pb = pv & 1;
+        if (!warp_wait(&bars[kSFull0 + b], (s_count >> 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         float sv[kKeys];
-#pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c) {
-          uint32_t r32[32];
-          tmem_ld32(lane_addr + b * kKeys + c * 32, r32);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(r32[e]);
-        }
+        tmem_ld128(lane_addr + kColS + b * kKeys, sv);
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kSFree0 + b]);
-        // causal mask and row max (log2 units)
-        const int key0 = j * kKeys;
-        float mx = -INFINITY;
+        ++s_count;
+        // causal mask (only key tiles that reach past the tile's first row) and row max
+        const int key0 = key_tile(t, j) * kKeys;
+        if (key0 + kKeys - 1 > pos_min) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          const float x = (key0 + c <= pos) ? sv[c] * p.scale_log2 : -INFINITY;
-          sv[c] = x;
-          mx = fmaxf(mx, x);
+          for (int c = 0; c < kKeys; ++c)
+            if (key0 + c > pos) sv[c] = -INFINITY;
         }
-        if (j > 0) {
-          // PV_{j-1} must be done before O is touched or the P tile rewritten
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait_or_abort(&bars[kODone], o_count & 1, p.err, abort_flag));
-          ++o_count;
-          if (!ok) break;
-          tc_fence_after();
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+        // the P buffer written now was last read by PV two tiles back
+        if (pv >= 2 && !warp_wait(&bars[kODone0 + pb], ((pv >> 1) - 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (j == 0) {
+          m_used = mx;  // key 0 is visible to every row, so mx is finite
+        } else {
           const bool mine = mx > m_used + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, mine)) {  // tensor-memory access is warp-collective
+          if (__any_sync(0xffffffffu, mine)) {
+            // O must hold PV_{j-1} before it is rescaled (tensor memory access is warp-wide)
+            const uint32_t prev = pv - 1;
+            if (!warp_wait(&bars[kODone0 + (prev & 1)], (prev >> 1) & 1, p.err, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
             const float alpha = mine ? exp2_approx(m_used - mx) : 1.f;
             if (mine) m_used = mx;
             l *= alpha;
@@ -364,44 +408,51 @@ __global__ void __launch_bounds__(192, 1)
             }
             tmem_wait_st();
           }
-        } else {
-          m_used = mx;  // key 0 is visible to every row, so mx is finite
         }
-        // P row (bf16) into the swizzled P tile; l sums the rounded weights
+        // P = 2^(s * scale_log2 - m_used) as bf16 pairs into tensor memory
+        const float neg_m = -m_used;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < kKeys / 8; ++c) {
-          uint32_t w[4];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = exp2_approx(sv[c * 8 + 2 * e] - m_used);
-            const float p1 = exp2_approx(sv[c * 8 + 2 * e + 1] - m_used);
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = exp2_approx(fmaf(sv[half * 64 + 2 * e], sl2, neg_m));
+            const float p1 = exp2_approx(fmaf(sv[half * 64 + 2 * e + 1], sl2, neg_m));
+            l4[e & 3] += p0 + p1;
             w[e] = pack_bf16(p0, p1);
-            l += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xffff0000u);
           }
-          *reinterpret_cast<uint4*>(p_tile + (c >> 3) * kRegion + swz128(row, c & 7)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+          tmem_st32(lane_addr + kColP + pb * 64 + half * 32, w);
         }
-        // keys past the request's end: zero this row's V so 0 * (stale) stays 0
-        if (j == t.nkt - 1 && key0 + row >= t.nkeys) {
-          uint8_t* vrow = smem + L::kKV + s * L::kKVStage + L::kKVHalf + row * 128;
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        tmem_wait_st();
+        // keys past the tile's last row: zero their V rows so 0 * (stale) stays 0
+        if (key0 + kKeys > t.nkeys) {
+          const int vs = v_count % kVStages;
+          if (!warp_wait(&bars[kVFull0 + vs], (v_count / kVStages) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (key0 + row >= t.nkeys) {
+            uint8_t* vrow = smem + L::kV + vs * L::kHalf + row * 128;
 #pragma unroll
-          for (int dh = 0; dh < NDH; ++dh)
+            for (int dh = 0; dh < NDH; ++dh)
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(vrow + dh * kRegion + c * 16) = make_uint4(0, 0, 0, 0);
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(vrow + dh * kRegion + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
+        ++v_count;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kPFull]);
-        ++s_count;
-        ++kv_count;
+        if (lane == 0) mbar_arrive(&bars[kPFull0 + pb]);
+        ++pv;
       }
       if (!ok) break;
-      // ---- epilogue: O / l -> out ----
-      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bars[kODone], o_count & 1, p.err, abort_flag)))
-        break;
-      ++o_count;
+      // ---- epilogue: O / l -> out, after the tile's last PV ----
+      const uint32_t last = pv - 1;
+      if (!warp_wait(&bars[kODone0 + (last & 1)], (last >> 1) & 1, p.err, abort_flag)) break;
       tc_fence_after();
       const float inv = 1.f / l;
       __nv_bfloat16* orow =
@@ -433,8 +484,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Encodes the [T, H, D] query as a 3-D tensor (D, H, T) with a box of
-// 64 dims x G heads x 128/G tokens, 128-byte swizzled.
 template <int D>
 static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap& qmap,
                                     const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
