@@ -113,9 +113,11 @@ int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride
  * max_query_len: host hint, >= every request's query length, or 0 if
  *   unknown; a value <= 1 skips the prefill launch.
  * workspace: device scratch of at least pkv_attention_workspace_bytes()
- *   bytes, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves it ready for
- *   the next one.  Word 0 is the error word (PKV_ERR_* bits, OR-ed in).  Two
- *   calls that overlap on the GPU must not share a workspace.
+ *   bytes for this batch, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves
+ *   it ready for the next one, including calls with a different number of
+ *   requests (its layout follows the largest batch it can hold).  Word 0 is
+ *   the error word (PKV_ERR_* bits, OR-ed in).  Two calls that overlap on the
+ *   GPU must not share a workspace.
  * ---------------------------------------------------------------------- */
 size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_t head_dim);
 

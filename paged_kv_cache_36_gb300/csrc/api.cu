@@ -36,6 +36,30 @@ WorkspaceLayout workspace_layout(int32_t num_reqs, int32_t num_heads, int32_t he
   return w;
 }
 
+// The layout a call uses is the one of the largest batch the workspace can
+// hold, not of the call's own batch: the split counters must sit at the same
+// place in every call that shares a workspace, or the partials of a small
+// batch would land on counters a later, larger batch expects to find zero.
+bool layout_for_capacity(size_t bytes, int32_t num_reqs, int32_t num_heads, int32_t head_dim,
+                         int grid, WorkspaceLayout* out) {
+  if (workspace_layout(num_reqs, num_heads, head_dim, grid).total > bytes) return false;
+  int64_t lo = num_reqs, hi = num_reqs;  // layout(lo) fits
+  while (hi < (int64_t(1) << 30) &&
+         workspace_layout(static_cast<int32_t>(hi * 2 + 1), num_heads, head_dim, grid).total <= bytes)
+    hi = hi * 2 + 1;
+  hi = hi * 2 + 2;                        // layout(hi) does not fit (or hi is past the search)
+  while (hi - lo > 1) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (mid < (int64_t(1) << 30) &&
+        workspace_layout(static_cast<int32_t>(mid), num_heads, head_dim, grid).total <= bytes)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  *out = workspace_layout(static_cast<int32_t>(lo), num_heads, head_dim, grid);
+  return true;
+}
+
 int current_grid() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -162,9 +186,10 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
     return fail(PKV_E_UNSUPPORTED, "pool of %lld blocks is too large", static_cast<long long>(num_blocks));
   if (!workspace) return fail(PKV_E_WORKSPACE, "workspace is required");
   const int grid = current_grid();
-  const WorkspaceLayout wl = workspace_layout(num_reqs, num_heads, head_dim, grid);
-  if (workspace_bytes < wl.total)
-    return fail(PKV_E_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, wl.total);
+  WorkspaceLayout wl;
+  if (!layout_for_capacity(workspace_bytes, num_reqs, num_heads, head_dim, grid, &wl))
+    return fail(PKV_E_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                workspace_layout(num_reqs, num_heads, head_dim, grid).total);
   if (num_tokens == 0 || num_reqs == 0) return PKV_OK;
   if (!q || !key_cache || !value_cache || !block_table || !query_start_loc || !seq_lens ||
       !num_computed_tokens || !out)

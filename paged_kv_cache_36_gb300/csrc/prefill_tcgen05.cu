@@ -68,6 +68,11 @@ enum Bar {
   kNumBars
 };
 
+static_assert(kKFull0 + kKStages == kKEmpty0 && kKEmpty0 + kKStages == kVFull0,
+              "one full and one empty barrier per K stage");
+static_assert(kVFull0 + kVStages == kVEmpty0 && kVEmpty0 + kVStages == kSFull0,
+              "one full and one empty barrier per V stage");
+
 struct PrefillParams {
   const int32_t* block_table;
   int32_t bt_stride;
@@ -270,7 +275,17 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
       uint32_t q_count = 0, k_count = 0, v_count = 0, s_count = 0, pv = 0;
-      const uint32_t q_base = smem_u32(smem + L::kQ);
+      // Descriptors are built once; a k-step only adds its byte offset >> 4 to
+      // the start-address field (all of shared memory fits in its 14 bits), so
+      // the issuing thread keeps up with the tensor core.
+      const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      uint64_t k_desc[kKStages], v_desc[kVStages];
+#pragma unroll
+      for (int i = 0; i < kKStages; ++i)
+        k_desc[i] = smem_desc_sw128(smem_u32(smem + L::kK + i * L::kHalf), 16, 1024);
+#pragma unroll
+      for (int i = 0; i < kVStages; ++i)
+        v_desc[i] = smem_desc_sw128(smem_u32(smem + L::kV + i * L::kHalf), kRegion, 1024);
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
         const Tile t = decode_tile(tile, prefix, R, p, tpt);
@@ -280,45 +295,47 @@ __global__ void __launch_bounds__(192, 1)
         long long t0 = clock64();
         while (ok && jp < t.nkt) {
           bool progressed = false;
-          if (jq < t.nkt && jq < jp + 2) {
-            const int ks = k_count % kKStages;
-            const int b = s_count & 1;
-            if (mbar_try_wait(&bars[kKFull0 + ks], (k_count / kKStages) & 1) &&
-                ((s_count >> 1) == 0 || mbar_try_wait(&bars[kSFree0 + b], ((s_count >> 1) - 1) & 1))) {
-              tc_fence_after();
-              const uint32_t k_base = smem_u32(smem + L::kK + ks * L::kHalf);
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-                tc_mma_ss(tmem + kColS + b * kKeys, smem_desc_sw128(q_base + off, 16, 1024),
-                          smem_desc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0);
-              }
-              tc_commit(&bars[kSFull0 + b]);
-              tc_commit(&bars[kKEmpty0 + ks]);
-              ++k_count;
-              ++s_count;
-              ++jq;
-              progressed = true;
-            }
-          }
+          // PV first when it can go: it is what the softmax waits for
           if (jp < jq) {
             const int pb = pv & 1;
             const int vs = v_count % kVStages;
-            if (mbar_try_wait(&bars[kPFull0 + pb], (pv >> 1) & 1) &&
-                mbar_try_wait(&bars[kVFull0 + vs], (v_count / kVStages) & 1)) {
+            if (mbar_test(&bars[kPFull0 + pb], (pv >> 1) & 1) &&
+                mbar_test(&bars[kVFull0 + vs], (v_count / kVStages) & 1)) {
               tc_fence_after();
-              const uint32_t v_base = smem_u32(smem + L::kV + vs * L::kHalf);
+              const uint64_t vd = v_desc[vs];
+              const uint32_t a_p = tmem + kColP + pb * 64;
+              const uint32_t first = jp > 0 ? 1u : 0u;
 #pragma unroll
               for (int kk = 0; kk < kKeys / 16; ++kk)
-                tc_mma_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8,
-                          smem_desc_sw128(v_base + kk * 16 * 128, kRegion, 1024), idesc_o,
-                          (jp > 0 || kk > 0) ? 1u : 0u);
+                tc_mma_ts(tmem + kColO, a_p + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_o,
+                          kk > 0 ? 1u : first);
               tc_commit(&bars[kODone0 + pb]);
               tc_commit(&bars[kVEmpty0 + vs]);
               ++v_count;
               ++pv;
               ++jp;
               if (jp == t.nkt) tc_commit(&bars[kQEmpty]);
+              progressed = true;
+            }
+          }
+          if (!progressed && jq < t.nkt && jq < jp + 2) {
+            const int ks = k_count % kKStages;
+            const int b = s_count & 1;
+            if (mbar_test(&bars[kKFull0 + ks], (k_count / kKStages) & 1) &&
+                ((s_count >> 1) == 0 || mbar_test(&bars[kSFree0 + b], ((s_count >> 1) - 1) & 1))) {
+              tc_fence_after();
+              const uint64_t kd = k_desc[ks];
+              const uint32_t d_s = tmem + kColS + b * kKeys;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = ((kk >> 2) * kRegion + (kk & 3) * 32) >> 4;
+                tc_mma_ss(d_s, q_desc + off, kd + off, idesc_s, kk > 0);
+              }
+              tc_commit(&bars[kSFull0 + b]);
+              tc_commit(&bars[kKEmpty0 + ks]);
+              ++k_count;
+              ++s_count;
+              ++jq;
               progressed = true;
             }
           }

@@ -197,6 +197,34 @@ def test_workspace_reuse_and_error_word():
     assert torch.equal(first, third)
 
 
+def test_workspace_shared_across_batch_sizes():
+    # one workspace serves batches of different sizes in any order: the split
+    # counters must not move with the batch size
+    pkv = _pkv()
+    H, Hkv, D = 32, 8, 128
+    batches = []
+    for i, ctx in enumerate([[3000, 5000, 800, 4000, 2500, 9000, 700, 6000, 100, 3300],
+                             [7000, 90, 4100], [1500] * 12 + [8000, 12000]]):
+        name = f"shared_ws_{i}"
+        counts = [(c + 15) // 16 for c in ctx]
+        NB = sum(counts) + 4
+        blocks = random_block_placement(NB, counts, name, "placement")
+        lengths = np.array(ctx, np.int64)
+        offsets = np.concatenate([[0], np.cumsum(lengths)[:-1]]).astype(np.int64)
+        kv = KVHistory(randn_fp32((int(lengths.sum()), Hkv, D), name, "k", dtype=torch.bfloat16),
+                       randn_fp32((int(lengths.sum()), Hkv, D), name, "v", dtype=torch.bfloat16),
+                       lengths, offsets)
+        q = randn_fp32((len(ctx), H, D), name, "q", dtype=torch.bfloat16)
+        b = Batch(kv, blocks, NB, [1] * len(ctx), [c - 1 for c in ctx], q, H, torch.bfloat16)
+        batches.append(b.alloc_cache().fill_history().upload_metadata().write_new_tokens())
+    fresh = [b.attention().clone() for b in batches]
+    ws = pkv.new_workspace(256, H, D)
+    for order in [0, 1, 2, 1, 0, 2, 2, 1]:
+        got = batches[order].attention(workspace=ws)
+        assert torch.equal(got, fresh[order]), order
+    compare(fresh[2], batches[2].oracle(), batches[2].qsl_host, torch.bfloat16)
+
+
 # ---------------------------------------------------------------- full-size configs
 def _decode_cfg_batch(cfg):
     return Batch(cfg.kv, cfg.blocks, cfg.num_blocks, np.ones(len(cfg.context), np.int64),

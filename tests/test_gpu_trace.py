@@ -1,0 +1,101 @@
+"""The continuous-batching trace on the GPU: 300 scheduler steps of Poisson
+arrivals with log-normal prompts and geometric outputs, token budget 8192,
+chunk size 512, max_num_seqs 256, a 16384-block pool (small enough that
+recompute preemption triggers), Llama-3-8B head shapes in bf16.
+
+Every step the C++ scheduler and the oracle scheduler are compared
+bit-exactly (plan, preemptions, admissions, block tables, slot mapping, free
+list), the step's tokens go through reshape_and_cache and paged attention on
+the GPU, and every CHECK_EVERY-th step the attention output of every request
+is compared with the float64 oracle over the request's own logical K/V
+history.  K/V rows are a function of (request, position) only, so a
+recomputed request rewrites identical values.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle.scheduler import NaiveScheduler, SchedConfig
+from tests.gpu_support import compare
+from workloads import PooledRows, generate_arrivals, trace_spec
+
+pytestmark = pytest.mark.gpu
+CHECK_EVERY = 20
+
+
+def test_trace_300_steps():
+    import paged_kv_cache_36_gb300 as pkv
+    spec = trace_spec()
+    H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    mbpr = spec.max_model_len // B
+    c = SchedConfig(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                    spec.max_model_len, B, spec.num_blocks, mbpr)
+    ref = NaiveScheduler(c, deep_checks=False)
+    cpp = pkv.Scheduler(c.max_num_seqs, c.max_num_batched_tokens, c.chunk_size, c.max_model_len,
+                        B, c.num_blocks, mbpr)
+    kv_rows = PooledRows(Hkv * D, "trace_kv")
+    q_rows = PooledRows(H * D, "trace_q")
+    kc = torch.zeros(spec.num_blocks, B, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ws = pkv.new_workspace(spec.max_num_seqs, H, D)
+    hist = {}          # rid -> (keys, values) of positions 0..len-1, host bf16
+    by_step = {}
+    for a in generate_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    checked = preemptions = 0
+    for step in range(spec.steps):
+        for a in by_step.get(step, []):
+            assert cpp.add_request(a.req_id, a.prompt_len, a.max_output) == \
+                ref.add_request(a.req_id, a.prompt_len, a.max_output)
+        pc, pr = cpp.step(), ref.step()
+        assert pc["entries"] == pr.entries and pc["preempted"] == pr.preempted
+        assert pc["admitted"] == pr.admitted
+        for rid in pr.preempted:
+            hist.pop(rid, None)
+            preemptions += 1
+        bt, qsl, seq, nc, slots = cpp.metadata()
+        rqsl, rseq, rnc, rrows, rslots = ref.metadata(pr)
+        assert qsl.tolist() == rqsl and seq.tolist() == rseq and nc.tolist() == rnc
+        assert slots.tolist() == rslots
+        for k, row in enumerate(rrows):
+            assert bt[k, :len(row)].tolist() == row
+        if step % 25 == 0:
+            assert cpp.allocator.free_list() == ref.alloc.free_list
+        T = int(qsl[-1])
+        if T:
+            rid_of = np.repeat([e[0] for e in pr.entries], [e[1] for e in pr.entries])
+            pos = np.concatenate([np.arange(e[2], e[2] + e[1]) for e in pr.entries])
+            kn = kv_rows.rows(0, rid_of, pos).view(T, Hkv, D)
+            vn = kv_rows.rows(1, rid_of, pos).view(T, Hkv, D)
+            q = q_rows.rows(2, np.full(T, step), np.arange(T)).view(T, H, D)
+            at = 0
+            for rid, s, ncb in pr.entries:
+                if ncb == 0:
+                    hist[rid] = (kn[at:at + s].clone(), vn[at:at + s].clone())
+                else:
+                    k0, v0 = hist[rid]
+                    assert k0.shape[0] == ncb
+                    hist[rid] = (torch.cat([k0, kn[at:at + s]]), torch.cat([v0, vn[at:at + s]]))
+                at += s
+            pkv.reshape_and_cache(kn.cuda(), vn.cuda(), kc, vc, torch.from_numpy(slots).cuda())
+            out = pkv.paged_attention_varlen(
+                q.cuda(), kc, vc, torch.from_numpy(bt).cuda(), torch.from_numpy(qsl).cuda(),
+                torch.from_numpy(seq).cuda(), torch.from_numpy(nc).cuda(), 1.0 / math.sqrt(D),
+                workspace=ws, max_query_len=pc["max_query_len"])
+            if step % CHECK_EVERY == 0:
+                histories = [hist[rid] for rid, _, _ in pr.entries]
+                want = oa.paged_attention_varlen(q, histories, qsl, seq, nc, 1.0 / math.sqrt(D))
+                compare(out, want, qsl, torch.bfloat16)
+                assert pkv.read_error_word(ws) == 0
+                checked += 1
+        fin_c, fin_r = cpp.finish_step(True), ref.finish_step(True)
+        assert fin_c == fin_r
+        for rid in fin_r:
+            hist.pop(rid, None)
+    torch.cuda.synchronize()
+    assert pkv.read_error_word(ws) == 0
+    assert preemptions > 0 and checked >= spec.steps // CHECK_EVERY - 1

@@ -8,7 +8,7 @@ attention.  Those live separately in the CUDA library and in the oracle.
 """
 
 from .generators import (  # noqa: F401
-    CounterKV,
+    PooledRows,
     randn_fp32,
     random_block_placement,
     uniform_int,

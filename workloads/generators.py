@@ -6,12 +6,12 @@ its own, independent of the order in which others are drawn).  Large tensors
 are drawn in fixed-size chunks on a thread pool; each chunk has its own seed
 list, so the result does not depend on the number of threads.
 
-`CounterKV` is a counter-based generator: the key/value/query vector of
-(request, position) is a pure function of its coordinates, so a request whose
-cache was dropped and is later recomputed writes bit-identical values, as a
-real model would.  It is splitmix64 (Steele, Lea and Flood, "Fast splittable
-pseudorandom number generators", OOPSLA 2014) feeding the Box-Muller
-transform.
+`PooledRows` gives the key/value/query vector of (request, position) as a
+pure function of its coordinates, so a request whose cache was dropped and is
+later recomputed writes bit-identical values, as a real model would.  The
+coordinates are hashed with splitmix64 (Steele, Lea and Flood, "Fast
+splittable pseudorandom number generators", OOPSLA 2014) into a seeded pool of
+N(0,1) rows.
 """
 
 from __future__ import annotations
@@ -90,7 +90,7 @@ def random_block_placement(pool_blocks: int, counts, *name) -> list[np.ndarray]:
 
 
 # ---------------------------------------------------------------------------
-# counter-based generator
+# counter-hashed row pools
 # ---------------------------------------------------------------------------
 _M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
 _GOLD = np.uint64(0x9E3779B97F4A7C15)
@@ -106,31 +106,32 @@ def _splitmix64(x: np.ndarray) -> np.ndarray:
         return z ^ (z >> np.uint64(31))
 
 
-class CounterKV:
-    """Deterministic N(0,1) vectors indexed by (stream, request, position).
+class PooledRows:
+    """Reproducible N(0,1) rows indexed by (stream, a, b), drawn from a pool.
 
-    stream is 0 for keys, 1 for values and 2 for queries.  `rows(stream, req,
-    positions, width)` returns float32 [len(positions), width]; element
-    (p, e) depends only on (seed, stream, req, p, e).
+    A pool of `pool_rows` rows of `width` float32 N(0,1) draws is generated
+    once (seeded).  The row for (stream, a, b) - e.g. (key, request, position)
+    - is pool[splitmix64(seed, stream, a, b) mod pool_rows], so the same
+    coordinates always give the same row: a request whose cache was dropped
+    and is recomputed writes bit-identical keys and values, as a real model
+    would.  Lookups are a vectorised hash and a gather, fast enough for
+    thousands of tokens per step.
     """
 
-    def __init__(self, seed: int = SEED):
-        self.seed = np.uint64(seed)
+    def __init__(self, width: int, name: str, pool_rows: int = 1 << 16, dtype=torch.bfloat16):
+        self.width = width
+        self.pool = randn_fp32((pool_rows, width), name, "pool", dtype=dtype)
+        self.n = pool_rows
+        self.key = int(_splitmix64(np.array([_seed_list(SEED, name)[1]], dtype=np.uint64))[0])
 
-    def rows(self, stream: int, req: int, positions, width: int) -> np.ndarray:
-        pos = np.asarray(positions, dtype=np.uint64).reshape(-1, 1)
-        half = (width + 1) // 2
-        e = np.arange(half, dtype=np.uint64).reshape(1, -1)
+    def index(self, stream: int, a, b) -> np.ndarray:
+        a = np.asarray(a, dtype=np.uint64)
+        b = np.asarray(b, dtype=np.uint64)
         with np.errstate(over="ignore"):
-            key = _splitmix64(self.seed ^ (np.uint64(stream) << np.uint64(56))
-                              ^ (np.uint64(req) << np.uint64(32)))
-            ctr = key + pos * np.uint64(1 << 20) + e
-        bits = _splitmix64(ctr)
-        # two 32-bit uniforms per 64-bit draw; u1 in (0, 1], u2 in [0, 1)
-        u1 = ((bits >> np.uint64(32)).astype(np.float64) + 1.0) / 4294967296.0
-        u2 = (bits & np.uint64(0xFFFFFFFF)).astype(np.float64) / 4294967296.0
-        r = np.sqrt(-2.0 * np.log(u1))
-        z = np.empty((pos.shape[0], 2 * half), dtype=np.float64)
-        z[:, 0::2] = r * np.cos(2.0 * np.pi * u2)
-        z[:, 1::2] = r * np.sin(2.0 * np.pi * u2)
-        return z[:, :width].astype(np.float32)
+            x = (np.uint64(self.key) ^ (np.uint64(stream) << np.uint64(60))
+                 ^ (a << np.uint64(32)) ^ b)
+            h = _splitmix64(x)
+        return (h % np.uint64(self.n)).astype(np.int64)
+
+    def rows(self, stream: int, a, b) -> torch.Tensor:
+        return self.pool[torch.from_numpy(self.index(stream, a, b))]
