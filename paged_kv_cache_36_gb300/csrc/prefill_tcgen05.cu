@@ -12,27 +12,28 @@
 // tiles of 128 = eight 16-token paged blocks; each block is one TMA box per
 // 64-dim half, landing 128-byte swizzled so that the 8 boxes form one
 // [128 keys x 64 dims] operand region.  Per key tile j:
-//   S_j = Q K_j^T   tcgen05.mma M=128 N=128 K=D, both operands in shared
-//                   memory, fp32 result in tensor memory (double-buffered)
-//   softmax        one thread per row reads its S row from tensor memory,
-//                   applies the causal mask on absolute positions, updates the
-//                   running max and sum, and writes P (bf16) back into tensor
-//                   memory (double-buffered)
-//   O  += P_j V_j  tcgen05.mma with A = P from tensor memory, B = V read
-//                   MN-major from shared memory, O in tensor memory
-// With S and P both double-buffered, QK^T of tile j+1 and PV of tile j-1 run
-// on the tensor core while the softmax of tile j runs.  A row's running max is
-// only moved (and its O, l rescaled) when the new max exceeds the one in use
-// by more than 2^8; otherwise the stale max keeps P <= 256, which is the same
-// arithmetic with a different reference point.
+//   S_j = Q K_j^T   tcgen05.mma M=128 N=128 K=D from shared memory, fp32 in
+//                   tensor memory (two S buffers)
+//   softmax        eight warps, two per 32-lane quadrant of tensor memory:
+//                   warp half h owns keys [64h, 64h + 64) of every tile, keeps
+//                   its own running max and sum, and writes its P (bf16) back
+//                   over the S columns it has just read
+//   O_h += P_h V_h tcgen05.mma with A = P from tensor memory and B = V rows
+//                   [64h, 64h + 64) read MN-major from shared memory
+// The two halves are two independent online softmaxes over disjoint key sets;
+// the epilogue merges them exactly: with M = max(m_0, m_1) and w_h =
+// 2^(m_h - M), out = (w_0 O_0 + w_1 O_1) / (w_0 l_0 + w_1 l_1).  A running
+// max is only moved (and its O, l rescaled) when it would grow by more than
+// 2^8; otherwise the stale max keeps P <= 256, the same arithmetic with a
+// different reference point.
 //
-// Warp roles (6 warps): warp 0 issues TMA (Q once per tile, K through a
-// 3-stage ring, V through a 2-stage ring), warp 1 owns the tensor memory and
-// issues MMAs from one thread, warps 2-5 (one per 32-lane quadrant of tensor
-// memory) run the softmax and the epilogue.  Tiles are handed out
-// persistently by a device-side plan over query_start_loc.  Every wait is
-// bounded; a timeout sets PKV_ERR_TIMEOUT and an abort flag that stops all
-// roles.
+// Warp roles (12 warps): warp 0 lane 0 streams Q and K (3-stage ring) and
+// lane 1 streams V (2-stage ring); warp 1 owns the tensor memory and issues
+// QK^T; warp 2 issues PV; warps 4-11 run the softmax and the epilogue.  Each
+// issuer blocks on its own barriers, so neither waits behind the other.
+// Tiles are handed out persistently by a device-side plan over
+// query_start_loc.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
+// an abort flag that stops all roles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -52,11 +53,13 @@ constexpr uint32_t kRegion = 16384;  // 128 rows x 128 bytes
 constexpr uint32_t kBox = 2048;      // 16 rows x 128 bytes
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-// tensor memory columns: S0, S1 (fp32 128 each), P0, P1 (bf16 pairs, 64 each), O
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = (4 + kSoftmaxWarps) * 32;
+// tensor memory: S/P buffers 0 and 1 (128 fp32 columns each; a warp half's P
+// overwrites the first 32 of its own 64 S columns), O_0 and O_1 (D columns)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColP = 256;
-constexpr uint32_t kColO = 384;
+constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum Bar {
@@ -64,10 +67,9 @@ enum Bar {
   kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2,
   kVFull0, kVFull1, kVEmpty0, kVEmpty1,
   kSFull0, kSFull1, kSFree0, kSFree1,
-  kPFull0, kPFull1, kODone0, kODone1,
+  kPFull, kODone, kXchg,
   kNumBars
 };
-
 static_assert(kKFull0 + kKStages == kKEmpty0 && kKEmpty0 + kKStages == kVFull0,
               "one full and one empty barrier per K stage");
 static_assert(kVFull0 + kVStages == kVEmpty0 && kVEmpty0 + kVStages == kSFull0,
@@ -91,7 +93,6 @@ struct PrefillParams {
 
 struct Tile {
   int r, h, u0, ntok, nkeys, nkt;
-  int first;  // key tile processed first (see key_tile)
   int64_t qs;
   int nc;
 };
@@ -104,7 +105,8 @@ struct Layout {
   static constexpr uint32_t kK = kQ + kHalf;
   static constexpr uint32_t kV = kK + kKStages * kHalf;
   static constexpr uint32_t kBars = kV + kVStages * kHalf;
-  static constexpr uint32_t kMisc = kBars + 8 * kNumBars;  // tmem slot, abort flag
+  static constexpr uint32_t kXch = kBars + 8 * kNumBars;      // [2 parity][2 half][128 rows] x (m, l)
+  static constexpr uint32_t kMisc = kXch + 2 * 2 * 128 * 8;   // tmem slot, abort flag
   static constexpr uint32_t kPrefix = kMisc + 16;
 };
 
@@ -127,18 +129,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int32_t* prefix, int
   t.ntok = min(tpt, qlen - t.u0);
   t.nkeys = t.nc + t.u0 + t.ntok;  // keys up to the last row's position
   t.nkt = (t.nkeys + kKeys - 1) / kKeys;
-  // CTAs sharing a KV head start at different key tiles so they do not all
-  // read the same cache lines at once; the first tile must be visible to every
-  // row (key0 <= smallest position), so the first row max is finite.
-  t.first = qt % ((t.nc + t.u0) / kKeys + 1);
   return t;
-}
-
-// Key tile handled at step j of a tile: a rotation of 0..nkt-1 (the online
-// softmax does not depend on the order in which keys arrive).
-__device__ __forceinline__ int key_tile(const Tile& t, int j) {
-  const int k = t.first + j;
-  return k < t.nkt ? k : k - t.nkt;
 }
 
 // All lanes of the calling warp wait; the result is made warp-uniform.
@@ -150,7 +141,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                            const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -159,6 +150,7 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  float2* xch = reinterpret_cast<float2*>(smem + L::kXch);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kPrefix);
@@ -170,10 +162,8 @@ __global__ void __launch_bounds__(192, 1)
   const int tpt = kRows / G;  // query tokens per tile
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < kNumBars; ++b) {
-      const bool softmax_arrives = b == kSFree0 || b == kSFree1 || b == kPFull0 || b == kPFull1;
-      mbar_init(&bars[b], softmax_arrives ? 4u : 1u);
-    }
+    for (int b = 0; b < kNumBars; ++b)
+      mbar_init(&bars[b], (b == kPFull || b == kXchg) ? kSoftmaxWarps : 1u);
     fence_mbar_init();
     *abort_flag = 0;
     prefix[0] = 0;
@@ -236,7 +226,7 @@ __global__ void __launch_bounds__(192, 1)
         const int nblk = (t.nkeys + 15) / 16;
         bool ok = true;
         for (int j = 0; j < t.nkt && ok; ++j) {
-          const int b0 = key_tile(t, j) * 8;
+          const int b0 = j * 8;
           const int nvalid = min(8, nblk - b0);
           int32_t phys[8];
 #pragma unroll
@@ -268,96 +258,88 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    // ============================ MMA issuer ============================
-    // One thread issues S_j = Q K_j^T and O += P_j V_j in whatever order their
-    // inputs become ready (QK may run up to two tiles ahead of PV).
+    // ============================ QK^T issuer ============================
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
-      uint32_t q_count = 0, k_count = 0, v_count = 0, s_count = 0, pv = 0;
-      // Descriptors are built once; a k-step only adds its byte offset >> 4 to
-      // the start-address field (all of shared memory fits in its 14 bits), so
-      // the issuing thread keeps up with the tensor core.
+      // descriptors are built once; a stage or k-step only adds its byte
+      // offset >> 4 to the start-address field
       const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
-      uint64_t k_desc[kKStages], v_desc[kVStages];
-#pragma unroll
-      for (int i = 0; i < kKStages; ++i)
-        k_desc[i] = smem_desc_sw128(smem_u32(smem + L::kK + i * L::kHalf), 16, 1024);
-#pragma unroll
-      for (int i = 0; i < kVStages; ++i)
-        v_desc[i] = smem_desc_sw128(smem_u32(smem + L::kV + i * L::kHalf), kRegion, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      uint32_t q_count = 0, k_count = 0, s_count = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
         const Tile t = decode_tile(tile, prefix, R, p, tpt);
         ok = mbar_wait_or_abort(&bars[kQFull], q_count & 1, p.err, abort_flag);
         ++q_count;
-        int jq = 0, jp = 0;  // next QK, next PV of this tile
-        long long t0 = clock64();
-        while (ok && jp < t.nkt) {
-          bool progressed = false;
-          // PV first when it can go: it is what the softmax waits for
-          if (jp < jq) {
-            const int pb = pv & 1;
-            const int vs = v_count % kVStages;
-            if (mbar_test(&bars[kPFull0 + pb], (pv >> 1) & 1) &&
-                mbar_test(&bars[kVFull0 + vs], (v_count / kVStages) & 1)) {
-              tc_fence_after();
-              const uint64_t vd = v_desc[vs];
-              const uint32_t a_p = tmem + kColP + pb * 64;
-              const uint32_t first = jp > 0 ? 1u : 0u;
+        for (int j = 0; j < t.nkt && ok; ++j) {
+          const int ks = k_count % kKStages;
+          const int b = s_count & 1;
+          ok = mbar_wait_or_abort(&bars[kKFull0 + ks], (k_count / kKStages) & 1, p.err, abort_flag);
+          // S/P buffer b is free once PV of the tile that last used it is done
+          if (ok && (s_count >> 1) > 0)
+            ok = mbar_wait_or_abort(&bars[kSFree0 + b], ((s_count >> 1) - 1) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kd = k_desc0 + ((ks * L::kHalf) >> 4);
+          const uint32_t d_s = tmem + kColS + b * kKeys;
 #pragma unroll
-              for (int kk = 0; kk < kKeys / 16; ++kk)
-                tc_mma_ts(tmem + kColO, a_p + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_o,
-                          kk > 0 ? 1u : first);
-              tc_commit(&bars[kODone0 + pb]);
-              tc_commit(&bars[kVEmpty0 + vs]);
-              ++v_count;
-              ++pv;
-              ++jp;
-              if (jp == t.nkt) tc_commit(&bars[kQEmpty]);
-              progressed = true;
-            }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = ((kk >> 2) * kRegion + (kk & 3) * 32) >> 4;
+            tc_mma_ss(d_s, q_desc + off, kd + off, idesc_s, kk > 0);
           }
-          if (!progressed && jq < t.nkt && jq < jp + 2) {
-            const int ks = k_count % kKStages;
-            const int b = s_count & 1;
-            if (mbar_test(&bars[kKFull0 + ks], (k_count / kKStages) & 1) &&
-                ((s_count >> 1) == 0 || mbar_test(&bars[kSFree0 + b], ((s_count >> 1) - 1) & 1))) {
-              tc_fence_after();
-              const uint64_t kd = k_desc[ks];
-              const uint32_t d_s = tmem + kColS + b * kKeys;
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = ((kk >> 2) * kRegion + (kk & 3) * 32) >> 4;
-                tc_mma_ss(d_s, q_desc + off, kd + off, idesc_s, kk > 0);
-              }
-              tc_commit(&bars[kSFull0 + b]);
-              tc_commit(&bars[kKEmpty0 + ks]);
-              ++k_count;
-              ++s_count;
-              ++jq;
-              progressed = true;
-            }
-          }
-          if (progressed) {
-            t0 = clock64();
-          } else if (*abort_flag) {
-            ok = false;
-          } else if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(p.err, PKV_ERR_TIMEOUT);
-            *abort_flag = 1;
-            ok = false;
-          }
+          tc_commit(&bars[kSFull0 + b]);
+          tc_commit(&bars[kKEmpty0 + ks]);
+          if (j == t.nkt - 1) tc_commit(&bars[kQEmpty]);
+          ++k_count;
+          ++s_count;
         }
       }
     }
-  } else {
+  } else if (warp == 2) {
+    // ============================ PV issuer ============================
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
+      const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + L::kV), kRegion, 1024);
+      uint32_t v_count = 0, s_count = 0, p_count = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, prefix, R, p, tpt);
+        for (int j = 0; j < t.nkt && ok; ++j) {
+          const int vs = v_count % kVStages;
+          const int b = s_count & 1;
+          ok = mbar_wait_or_abort(&bars[kPFull], p_count & 1, p.err, abort_flag) &&
+               mbar_wait_or_abort(&bars[kVFull0 + vs], (v_count / kVStages) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + ((vs * L::kHalf) >> 4);
+          const uint32_t a_p = tmem + kColS + b * kKeys;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t d_o = tmem + kColO + half * D;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ts(d_o, a_p + half * 64 + kk * 8,
+                        vd + (((half * 64 + kk * 16) * 128) >> 4), idesc_o,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&bars[kODone]);
+          tc_commit(&bars[kSFree0 + b]);
+          tc_commit(&bars[kVEmpty0 + vs]);
+          ++v_count;
+          ++s_count;
+          ++p_count;
+        }
+      }
+    }
+  } else if (warp >= 4) {
     // ============================ softmax warps ============================
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;  // tile row = tensor-memory lane
+    const int half = (warp - 4) >> 2;    // keys [64 half, 64 half + 64) of each tile
+    const int row = quad * 32 + lane;    // tile row = tensor-memory lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t o_cols = lane_addr + kColO + half * D;
     const float sl2 = p.scale_log2;
-    uint32_t s_count = 0, v_count = 0, pv = 0;
+    uint32_t s_count = 0, v_count = 0, o_count = 0, tiles_done = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Tile t = decode_tile(tile, prefix, R, p, tpt);
@@ -369,43 +351,38 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int j = 0; j < t.nkt && ok; ++j) {
         const int b = s_count & 1;
-        const int pb = pv & 1;
         if (!warp_wait(&bars[kSFull0 + b], (s_count >> 1) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float sv[kKeys];
-        tmem_ld128(lane_addr + kColS + b * kKeys, sv);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kSFree0 + b]);
+        const uint32_t s_cols = lane_addr + kColS + b * kKeys + half * 64;
+        float sv[64];
+        {
+          uint32_t (&r)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sv);
+          tmem_ld32(s_cols, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld32(s_cols + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_wait_ld();
+        }
         ++s_count;
-        // causal mask (only key tiles that reach past the tile's first row) and row max
-        const int key0 = key_tile(t, j) * kKeys;
-        if (key0 + kKeys - 1 > pos_min) {
+        // causal mask (only tiles reaching past the tile's first row) and max
+        const int key0 = j * kKeys + half * 64;
+        if (key0 + 63 > pos_min) {
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c)
+          for (int c = 0; c < 64; ++c)
             if (key0 + c > pos) sv[c] = -INFINITY;
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+        for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-        // the P buffer written now was last read by PV two tiles back
-        if (pv >= 2 && !warp_wait(&bars[kODone0 + pb], ((pv >> 1) - 1) & 1, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
         if (j == 0) {
-          m_used = mx;  // key 0 is visible to every row, so mx is finite
+          m_used = mx;  // may be -inf when this half sees no key yet
         } else {
           const bool mine = mx > m_used + kRescaleThreshold;
           if (__any_sync(0xffffffffu, mine)) {
-            // O must hold PV_{j-1} before it is rescaled (tensor memory access is warp-wide)
-            const uint32_t prev = pv - 1;
-            if (!warp_wait(&bars[kODone0 + (prev & 1)], (prev >> 1) & 1, p.err, abort_flag)) {
+            // O must hold PV of the previous tile before it is rescaled
+            if (!warp_wait(&bars[kODone], o_count & 1, p.err, abort_flag)) {
               ok = false;
               break;
             }
@@ -416,42 +393,42 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t r32[32];
-              tmem_ld32(lane_addr + kColO + c * 32, r32);
+              tmem_ld32(o_cols + c * 32, r32);
               tmem_wait_ld();
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 r32[e] = __float_as_uint(__uint_as_float(r32[e]) * alpha);
-              tmem_st32(lane_addr + kColO + c * 32, r32);
+              tmem_st32(o_cols + c * 32, r32);
             }
             tmem_wait_st();
           }
         }
-        // P = 2^(s * scale_log2 - m_used) as bf16 pairs into tensor memory
-        const float neg_m = -m_used;
+        if (j > 0) ++o_count;  // PV of tile j-1 is the o_done phase this tile may wait on
+        // P = 2^(s * scale_log2 - m_used) as bf16 pairs over the first 32 of
+        // this half's S columns (a row with no visible key yet gets P = 0)
+        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t w[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t w[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p0 = exp2_approx(fmaf(sv[half * 64 + 2 * e], sl2, neg_m));
-            const float p1 = exp2_approx(fmaf(sv[half * 64 + 2 * e + 1], sl2, neg_m));
-            l4[e & 3] += p0 + p1;
-            w[e] = pack_bf16(p0, p1);
-          }
-          tmem_st32(lane_addr + kColP + pb * 64 + half * 32, w);
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = exp2_approx(fmaf(sv[2 * e], sl2, neg_m));
+          const float p1 = exp2_approx(fmaf(sv[2 * e + 1], sl2, neg_m));
+          l4[e & 3] += p0 + p1;
+          w[e] = pack_bf16(p0, p1);
         }
+        tmem_st32(s_cols, w);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_wait_st();
         // keys past the tile's last row: zero their V rows so 0 * (stale) stays 0
-        if (key0 + kKeys > t.nkeys) {
+        if (j == t.nkt - 1 && j * kKeys + kKeys > t.nkeys) {
           const int vs = v_count % kVStages;
           if (!warp_wait(&bars[kVFull0 + vs], (v_count / kVStages) & 1, p.err, abort_flag)) {
             ok = false;
             break;
           }
-          if (key0 + row >= t.nkeys) {
-            uint8_t* vrow = smem + L::kV + vs * L::kHalf + row * 128;
+          const int key = j * kKeys + half * 64 + (quad & 1) * 32 + lane;
+          if (quad < 2 && key >= t.nkeys) {
+            uint8_t* vrow = smem + L::kV + vs * L::kHalf + (key - j * kKeys) * 128;
 #pragma unroll
             for (int dh = 0; dh < NDH; ++dh)
 #pragma unroll
@@ -463,31 +440,50 @@ __global__ void __launch_bounds__(192, 1)
         ++v_count;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kPFull0 + pb]);
-        ++pv;
+        if (lane == 0) mbar_arrive(&bars[kPFull]);
       }
       if (!ok) break;
-      // ---- epilogue: O / l -> out, after the tile's last PV ----
-      const uint32_t last = pv - 1;
-      if (!warp_wait(&bars[kODone0 + (last & 1)], (last >> 1) & 1, p.err, abort_flag)) break;
+      // ---- epilogue: merge the two halves, O / l -> out ----
+      if (!warp_wait(&bars[kODone], o_count & 1, p.err, abort_flag)) break;
+      ++o_count;
       tc_fence_after();
-      const float inv = 1.f / l;
+      float2* mine_x = xch + ((tiles_done & 1) * 2 + half) * 128;
+      float2* other_x = xch + ((tiles_done & 1) * 2 + (half ^ 1)) * 128;
+      mine_x[row] = make_float2(m_used, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kXchg]);
+      if (!warp_wait(&bars[kXchg], tiles_done & 1, p.err, abort_flag)) break;
+      ++tiles_done;
+      const float2 o = other_x[row];
+      const float m0 = half == 0 ? m_used : o.x, l0 = half == 0 ? l : o.y;
+      const float m1 = half == 0 ? o.x : m_used, l1 = half == 0 ? o.y : l;
+      const float mm = fmaxf(m0, m1);  // finite: key 0 is visible to every row
+      const float w0 = exp2_approx(m0 - mm), w1 = exp2_approx(m1 - mm);
+      const float inv = 1.f / (w0 * l0 + w1 * l1);
+      const float c0 = w0 * inv, c1 = w1 * inv;
       __nv_bfloat16* orow =
           p.out + (t.qs + u) * p.out_stride + static_cast<int64_t>(t.h * G + row % G) * D;
+      // this warp writes output dims [half * D/2, half * D/2 + D/2)
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r32[32];
-        tmem_ld32(lane_addr + kColO + c * 32, r32);
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t col = half * (D / 2) + c * 32;
+        uint32_t r0[32], r1[32];
+        tmem_ld32(lane_addr + kColO + col, r0);
+        tmem_ld32(lane_addr + kColO + D + col, r1);
         tmem_wait_ld();
         if (valid_row) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              f[e] = __uint_as_float(r0[q4 * 8 + e]) * c0 + __uint_as_float(r1[q4 * 8 + e]) * c1;
             uint4 v;
-            v.x = pack_bf16(__uint_as_float(r32[q4 * 8 + 0]) * inv, __uint_as_float(r32[q4 * 8 + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(r32[q4 * 8 + 2]) * inv, __uint_as_float(r32[q4 * 8 + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(r32[q4 * 8 + 4]) * inv, __uint_as_float(r32[q4 * 8 + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(r32[q4 * 8 + 6]) * inv, __uint_as_float(r32[q4 * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = v;
+            v.x = pack_bf16(f[0], f[1]);
+            v.y = pack_bf16(f[2], f[3]);
+            v.z = pack_bf16(f[4], f[5]);
+            v.w = pack_bf16(f[6], f[7]);
+            *reinterpret_cast<uint4*>(orow + col + q4 * 8) = v;
           }
         }
       }
@@ -512,7 +508,7 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap&
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, 192, smem, stream>>>(qmap, kmap, vmap, prm);
+  kern<<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, prm);
   return cudaGetLastError();
 }
 
