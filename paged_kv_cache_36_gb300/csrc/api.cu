@@ -250,7 +250,7 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
     rc = encode_query_map(&qmap, q, q_stride, num_tokens, num_heads, num_heads / num_kv_heads,
                           head_dim);
     if (rc != PKV_OK) return rc;
-    e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, st);
+    e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   return PKV_OK;

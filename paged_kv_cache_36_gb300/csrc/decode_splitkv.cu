@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(288, 1)
   int32_t* prefix = reinterpret_cast<int32_t*>(empty_bar + p.stages);  // [R + 1]
   int32_t* scan_tmp = prefix + R + 1;                                   // [32]
 
+  // the prefill kernel launched after this one reads nothing it writes: let
+  // it be scheduled onto SMs as soon as they free up
+  if (threadIdx.x == 0) grid_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -447,9 +450,9 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, const CUtensorMap& k
                                    const CUtensorMap& vmap, int grid, size_t smem,
                                    cudaStream_t stream) {
   auto kern = decode_splitkv_kernel<D, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  const cudaError_t status = raise_smem_limit_once<decode_splitkv_kernel<D, NT>>(kSmemBudget);
+  if (status != cudaSuccess) return status;
+  if (smem > kSmemBudget) return cudaErrorNotSupported;
   kern<<<grid, (prm.hkv + 1) * 32, smem, stream>>>(kmap, vmap, prm);
   return cudaGetLastError();
 }

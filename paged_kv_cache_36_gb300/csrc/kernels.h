@@ -6,8 +6,28 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace pkv {
+
+// Raises the dynamic shared-memory limit of kernel `Kern` to `bytes`, once per
+// device (the attribute is per function and device; setting it on every launch
+// costs host time).
+template <auto Kern>
+cudaError_t raise_smem_limit_once(size_t bytes) {
+  constexpr int kDevices = 64;
+  static std::once_flag once[kDevices];
+  static cudaError_t status[kDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    status[dev] = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  });
+  return status[dev];
+}
 
 // Everything an attention kernel needs about one paged_attention_varlen call.
 struct AttnArgs {
@@ -58,7 +78,8 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const
 // with query length > 1; qmap is the [T, H, D] query as a (D, H, T) tensor map
 // with a 64 x G x 128/G box.
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int grid, cudaStream_t stream);
+                                const CUtensorMap& vmap, int sms, int max_query_len,
+                                cudaStream_t stream);
 
 // CUDA-core attention, one warp per (query row, head); fp32 path for all rows,
 // or only rows of requests with query length > 1 when skip_decode is set.

@@ -198,3 +198,18 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 }  // namespace pkv
+
+namespace pkv {
+
+// Programmatic dependent launch: let the next kernel in the stream, when it
+// was launched as a programmatic dependent, be scheduled before this one ends.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Block until the grids this one programmatically depends on have completed
+// and their memory operations are visible (returns at once otherwise).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace pkv

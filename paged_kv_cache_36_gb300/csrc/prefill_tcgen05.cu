@@ -34,10 +34,22 @@
 // Tiles are handed out persistently by a device-side plan over
 // query_start_loc.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
 // an abort flag that stops all roles.
+//
+// K/V sharing across a cluster.  With a cluster of C CTAs, the members take C
+// adjacent query tiles of the same (request, KV head) and walk the same key
+// tiles in lockstep: every K/V box lands in all members' shared memory by one
+// multicast TMA load, each member issuing 1/C of each tile's boxes, and a
+// stage is refilled only after all C members' MMAs have released it (the
+// release is a multicast tcgen05.commit onto every member's empty barrier).
+// This divides the L2->SM traffic and the TMA issue work per tile by C.  A
+// member walks the key tiles of the cluster's last query row; keys beyond its
+// own rows are masked.  A member past the request's last query tile recomputes
+// that tile without storing it, so the lockstep never breaks.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "kernels.h"
 #include "pkv_device.cuh"
@@ -61,6 +73,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr size_t kPrefillSmemLimit = 232448;  // 227 KiB per CTA
+constexpr int kMaxDevices = 64;
 
 enum Bar {
   kQFull, kQEmpty,
@@ -92,9 +106,12 @@ struct PrefillParams {
 };
 
 struct Tile {
-  int r, h, u0, ntok, nkeys, nkt;
+  int r, h, u0, ntok;
+  int nkeys;   // keys loaded for the cluster: up to its last query row's position
+  int nkt;     // key tiles walked by every member
   int64_t qs;
   int nc;
+  bool store;  // false for a member past the request's last query tile
 };
 
 template <int D>
@@ -110,24 +127,33 @@ struct Layout {
   static constexpr uint32_t kPrefix = kMisc + 16;
 };
 
-__device__ __forceinline__ Tile decode_tile(int tile, const int32_t* prefix, int R,
+// Cluster tile `ct` -> the query tile that cluster member `rank` computes.
+// prefix[r] counts the cluster tiles of requests before r; within a request
+// cluster tiles run KV head fastest, then groups of C query tiles.
+template <int C>
+__device__ __forceinline__ Tile decode_tile(int ct, int rank, const int32_t* prefix, int R,
                                             const PrefillParams& p, int tpt) {
-  int lo = 0, hi = R;  // prefix[lo] <= tile < prefix[hi]
+  int lo = 0, hi = R;  // prefix[lo] <= ct < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= tile) lo = mid; else hi = mid;
+    if (prefix[mid] <= ct) lo = mid; else hi = mid;
   }
   Tile t;
   t.r = lo;
-  const int rem = tile - prefix[lo];
-  const int qt = rem / p.hkv;
-  t.h = rem - qt * p.hkv;
+  const int rem = ct - prefix[lo];
+  const int grp = rem / p.hkv;
+  t.h = rem - grp * p.hkv;
   t.qs = __ldg(p.qsl + t.r);
   const int qlen = __ldg(p.qsl + t.r + 1) - static_cast<int>(t.qs);
   t.nc = __ldg(p.num_computed + t.r);
+  const int nqt = (qlen + tpt - 1) / tpt;
+  const int last = min(grp * C + C, nqt) - 1;  // the cluster's last real query tile
+  int qt = grp * C + rank;
+  t.store = qt <= last;
+  if (!t.store) qt = last;
   t.u0 = qt * tpt;
   t.ntok = min(tpt, qlen - t.u0);
-  t.nkeys = t.nc + t.u0 + t.ntok;  // keys up to the last row's position
+  t.nkeys = t.nc + min(qlen, last * tpt + tpt);
   t.nkt = (t.nkeys + kKeys - 1) / kKeys;
   return t;
 }
@@ -140,7 +166,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
 
 }  // namespace
 
-template <int D>
+template <int D, int C>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                            const __grid_constant__ CUtensorMap kmap,
@@ -158,12 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = p.num_reqs;
+  const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = blockIdx.x / C, ncl = gridDim.x / C;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << C) - 1);
   const int G = p.group;
   const int tpt = kRows / G;  // query tokens per tile
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < kNumBars; ++b)
-      mbar_init(&bars[b], (b == kPFull || b == kXchg) ? kSoftmaxWarps : 1u);
+    for (int b = 0; b < kNumBars; ++b) {
+      uint32_t n = 1;
+      if (b == kPFull || b == kXchg) n = kSoftmaxWarps;
+      if ((b >= kKEmpty0 && b < kKEmpty0 + kKStages) || (b >= kVEmpty0 && b < kVEmpty0 + kVStages))
+        n = C;  // released by the MMAs of every cluster member
+      mbar_init(&bars[b], n);
+    }
     fence_mbar_init();
     *abort_flag = 0;
     prefix[0] = 0;
@@ -186,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (seq != __ldg(p.num_computed + r) + qlen || (seq + 15) / 16 > p.bt_stride) {
         if (blockIdx.x == 0) atomicOr(p.err, PKV_ERR_METADATA);
       } else {
-        nt = ((qlen + tpt - 1) / tpt) * p.hkv;
+        nt = ((qlen + tpt - 1) / tpt + C - 1) / C * p.hkv;
       }
     }
     prefix[r + 1] = nt;
@@ -196,6 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   block_inclusive_scan(prefix + 1, R, scan_tmp);
   __syncthreads();
+  // every member's barriers are initialised before any multicast reaches them
+  if (C > 1) cluster_sync_all();
   const int total = prefix[R];
   const uint32_t tmem = *tmem_slot;
 
@@ -211,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* map = is_k ? &kmap : &vmap;
       uint8_t* ring = smem + (is_k ? L::kK : L::kV);
       uint32_t q_uses = 0, count = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, prefix, R, p, tpt);
+      for (int ct = cid; ct < total && !*abort_flag; ct += ncl) {
+        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
         if (is_k) {
           if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag))
             break;
@@ -246,16 +282,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&bars[full0 + st], NDH * kBox * nvalid);
           uint8_t* dst = ring + st * L::kHalf;
+          // box i = k * NDH + dh goes out from member i % C to all members
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             if (k < nvalid)
-              for (int dh = 0; dh < NDH; ++dh)
-                tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
-                            &bars[full0 + st]);
+              for (int dh = 0; dh < NDH; ++dh) {
+                if (C == 1) {
+                  tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
+                              &bars[full0 + st]);
+                } else if ((k * NDH + dh) % C == rank) {
+                  tma_load_3d_multicast(dst + dh * kRegion + k * kBox, map, dh * 64, t.h,
+                                        phys[k] * 16, &bars[full0 + st], kMask);
+                }
+              }
           ++count;
         }
         if (!ok) break;
       }
+      // drain: every copy into this CTA's ring (and, in a cluster, every
+      // member's release of it) has landed before the CTA may exit
+      for (int st = 0; st < nst; ++st) {
+        const uint32_t uses = count / nst + (static_cast<uint32_t>(st) < count % nst ? 1u : 0u);
+        if (uses == 0) continue;
+        mbar_wait(&bars[full0 + st], (uses - 1) & 1, p.err);
+        if (C > 1) mbar_wait(&bars[empty0 + st], (uses - 1) & 1, p.err);
+      }
+      if (is_k && q_uses > 0) mbar_wait(&bars[kQFull], (q_uses - 1) & 1, p.err);
     }
   } else if (warp == 1) {
     // ============================ QK^T issuer ============================
@@ -267,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
       uint32_t q_count = 0, k_count = 0, s_count = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, prefix, R, p, tpt);
+      for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
+        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
         ok = mbar_wait_or_abort(&bars[kQFull], q_count & 1, p.err, abort_flag);
         ++q_count;
         for (int j = 0; j < t.nkt && ok; ++j) {
@@ -288,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_ss(d_s, q_desc + off, kd + off, idesc_s, kk > 0);
           }
           tc_commit(&bars[kSFull0 + b]);
-          tc_commit(&bars[kKEmpty0 + ks]);
+          if (C == 1) tc_commit(&bars[kKEmpty0 + ks]);
+          else tc_commit_multicast(&bars[kKEmpty0 + ks], kMask);
           if (j == t.nkt - 1) tc_commit(&bars[kQEmpty]);
           ++k_count;
           ++s_count;
@@ -302,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + L::kV), kRegion, 1024);
       uint32_t v_count = 0, s_count = 0, p_count = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, prefix, R, p, tpt);
+      for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
+        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
         for (int j = 0; j < t.nkt && ok; ++j) {
           const int vs = v_count % kVStages;
           const int b = s_count & 1;
@@ -324,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(&bars[kODone]);
           tc_commit(&bars[kSFree0 + b]);
-          tc_commit(&bars[kVEmpty0 + vs]);
+          if (C == 1) tc_commit(&bars[kVEmpty0 + vs]);
+          else tc_commit_multicast(&bars[kVEmpty0 + vs], kMask);
           ++v_count;
           ++s_count;
           ++p_count;
@@ -340,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_cols = lane_addr + kColO + half * D;
     const float sl2 = p.scale_log2;
     uint32_t s_count = 0, v_count = 0, o_count = 0, tiles_done = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int ct = cid; ct < total; ct += ncl) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = decode_tile(tile, prefix, R, p, tpt);
+      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
       const int u = t.u0 + row / G;  // token of this row within the request
       const bool valid_row = (row / G) < t.ntok;
       const int pos = t.nc + (valid_row ? u : t.u0 + t.ntok - 1);
@@ -419,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(s_cols, w);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_wait_st();
-        // keys past the tile's last row: zero their V rows so 0 * (stale) stays 0
+        // keys past the cluster's last row were not loaded: zero their V rows
+        // so that 0 * (stale) stays 0
         if (j == t.nkt - 1 && j * kKeys + kKeys > t.nkeys) {
           const int vs = v_count % kVStages;
           if (!warp_wait(&bars[kVFull0 + vs], (v_count / kVStages) & 1, p.err, abort_flag)) {
@@ -471,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_addr + kColO + col, r0);
         tmem_ld32(lane_addr + kColO + D + col, r1);
         tmem_wait_ld();
-        if (valid_row) {
+        if (valid_row && t.store) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             float f[8];
@@ -494,26 +549,82 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (C > 1) cluster_sync_all();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  // launched as a programmatic dependent of the decode kernel: do not complete
+  // before it, so that work after this kernel sees both
+  if (threadIdx.x == 0) grid_dependency_wait();
 }
 
+// Shared memory of one CTA: the layout plus the per-request tile prefix.
 template <int D>
+static size_t prefill_smem_bytes(int num_reqs) {
+  return 1024 + Layout<D>::kPrefix + 4 * (static_cast<size_t>(num_reqs) + 1) + 4 * 32;
+}
+
+// Per device: how many clusters of an instantiation fit on the GPU at once.
+struct PrefillClusterCount {
+  std::once_flag once[kMaxDevices];
+  cudaError_t status[kMaxDevices];
+  int clusters[kMaxDevices];
+};
+
+template <int D, int C>
 static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap& qmap,
-                                    const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                                    const CUtensorMap& kmap, const CUtensorMap& vmap, int sms,
                                     cudaStream_t stream) {
-  using L = Layout<D>;
-  const size_t smem = 1024 + L::kPrefix + 4 * (prm.num_reqs + 1) + 4 * 32;
-  if (smem > 232448) return cudaErrorNotSupported;
-  auto kern = prefill_tcgen05_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const size_t smem = prefill_smem_bytes<D>(prm.num_reqs);
+  if (smem > kPrefillSmemLimit) return cudaErrorNotSupported;
+  auto kern = prefill_tcgen05_kernel<D, C>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, prm);
-  return cudaGetLastError();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  e = raise_smem_limit_once<prefill_tcgen05_kernel<D, C>>(kPrefillSmemLimit);
+  if (e != cudaSuccess) return e;
+  static PrefillClusterCount info;
+  std::call_once(info.once[dev], [&] {
+    info.clusters[dev] = sms / C;
+    info.status[dev] = cudaSuccess;
+    if (C == 1) return;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms / C * C));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kPrefillSmemLimit;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    info.status[dev] = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (info.status[dev] == cudaSuccess) info.clusters[dev] = n > 0 ? n : 1;
+  });
+  if (info.status[dev] != cudaSuccess) return info.status[dev];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // the prefill reads nothing the decode kernel before it writes, so it may be
+  // scheduled while that kernel drains; it waits for it only before exiting
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(info.clusters[dev] * C));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, prm);
 }
 
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int grid, cudaStream_t stream) {
+                                const CUtensorMap& vmap, int sms, int max_query_len,
+                                cudaStream_t stream) {
   const int G = a.num_heads / a.num_kv_heads;
   if (G > 128 || kRows % G) return cudaErrorNotSupported;
   PrefillParams prm;
@@ -530,8 +641,21 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, cons
   prm.group = G;
   prm.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   prm.err = a.err;
-  if (a.head_dim == 128) return launch_prefill_t<128>(prm, qmap, kmap, vmap, grid, stream);
-  if (a.head_dim == 64) return launch_prefill_t<64>(prm, qmap, kmap, vmap, grid, stream);
+  // clusters share K/V across query tiles of one request: as many members as
+  // the longest request has query tiles, up to 4
+  const int tpt = kRows / G;
+  const int qtiles = max_query_len > 0 ? (max_query_len + tpt - 1) / tpt : 4;
+  const int C = qtiles >= 4 ? 4 : qtiles >= 2 ? 2 : 1;
+  if (a.head_dim == 128) {
+    if (C == 4) return launch_prefill_t<128, 4>(prm, qmap, kmap, vmap, sms, stream);
+    if (C == 2) return launch_prefill_t<128, 2>(prm, qmap, kmap, vmap, sms, stream);
+    return launch_prefill_t<128, 1>(prm, qmap, kmap, vmap, sms, stream);
+  }
+  if (a.head_dim == 64) {
+    if (C == 4) return launch_prefill_t<64, 4>(prm, qmap, kmap, vmap, sms, stream);
+    if (C == 2) return launch_prefill_t<64, 2>(prm, qmap, kmap, vmap, sms, stream);
+    return launch_prefill_t<64, 1>(prm, qmap, kmap, vmap, sms, stream);
+  }
   return cudaErrorNotSupported;
 }
 

@@ -142,6 +142,15 @@ CASES = [
     (16, 2, 128, [1, 1, 2, 1], [513, 2, 77, 4095]),
     (64, 8, 128, [1, 1, 9], [2000, 31, 100]),
     (4, 1, 64, [1, 20, 1], [63, 16, 1000]),
+    # prefill rows spanning several query tiles, so that clusters of 2 and 4
+    # CTAs share K/V: query-tile counts that are not a multiple of the
+    # cluster size leave members past a request's last tile
+    (32, 8, 128, [70, 1, 45], [0, 10, 1000]),
+    (32, 8, 128, [300, 129, 1, 64], [0, 2500, 40, 7]),
+    (16, 4, 64, [200, 33], [5, 100]),
+    (64, 8, 128, [100, 1], [3000, 5]),
+    (16, 8, 128, [150], [17]),
+    (32, 2, 128, [40, 1], [60, 9]),
 ]
 
 
