@@ -27,9 +27,9 @@
 // 2^8; otherwise the stale max keeps P <= 256, the same arithmetic with a
 // different reference point.
 //
-// Warp roles (12 warps): warp 0 lane 0 streams Q and K (3-stage ring) and
-// lane 1 streams V (2-stage ring); warp 1 owns the tensor memory and issues
-// QK^T; warp 2 issues PV; warps 4-11 run the softmax and the epilogue.  Each
+// Warp roles (12 warps): warp 0 streams Q and K (3-stage ring), warp 3
+// streams V (2-stage ring); warp 1 owns the tensor memory and issues QK^T;
+// warp 2 issues PV; warps 4-11 run the softmax and the epilogue.  Each
 // issuer blocks on its own barriers, so neither waits behind the other.
 // Tiles are handed out persistently by a device-side plan over
 // query_start_loc.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
@@ -235,12 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = prefix[R];
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 3) {
     // ============================ TMA producers ============================
-    // lane 0 streams Q and K, lane 1 streams V; each runs its own loop (no
-    // warp-collective operations), so K can run ahead while V waits for PV.
-    if (lane < 2) {
-      const bool is_k = lane == 0;
+    // warp 0 streams Q and K, warp 3 streams V.  They are separate warps so
+    // that neither waits on the other's ring: two lanes of one warp would run
+    // converged, and K would stall whenever V waits for a free stage.
+    if (lane == 0) {
+      const bool is_k = warp == 0;
       const int nst = is_k ? kKStages : kVStages;
       const int full0 = is_k ? kKFull0 : kVFull0;
       const int empty0 = is_k ? kKEmpty0 : kVEmpty0;
