@@ -99,6 +99,54 @@ int encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int
   return PKV_OK;
 }
 
+// One paged block of one cache, all heads, as a single box: the 4-D view
+// (64 dims, num_blocks * block_size tokens, head_dim / 64 halves, num_kv_heads)
+// with strides (2 B, row, 128 B, head_dim * 2 B) and box (64, block_size,
+// head_dim / 64, num_kv_heads).  The box lands as [head][half][token][128 B],
+// 128-byte swizzled, so one copy fetches what 2 * num_kv_heads boxes of
+// encode_cache_map would.
+int encode_cache_block_map(CUtensorMap* map, const void* base, int64_t num_blocks,
+                           int32_t block_size, int32_t hkv, int32_t d) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t row = static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(hkv);
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(num_blocks * block_size),
+                        static_cast<cuuint64_t>(d / 64), static_cast<cuuint64_t>(hkv)};
+  cuuint64_t strides[3] = {row, 128, static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(block_size), static_cast<cuuint32_t>(d / 64),
+                       static_cast<cuuint32_t>(hkv)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled (block) failed (%d)", int(r));
+  return PKV_OK;
+}
+
+// One head of one 16-token paged block as a single box laid out for a
+// K-major tensor-core operand: the 5-D view (64 dims, 8 tokens, head_dim / 64
+// halves, num_kv_heads, num_blocks * 2 half-blocks) with strides (2 B, row,
+// 128 B, head_dim * 2 B, 8 rows) and box (64, 8, head_dim / 64, 1, 2).  The
+// box lands as [token half][dim half][8 tokens][128 B]: consecutive groups of
+// 8 keys sit head_dim / 64 KiB apart whichever dim half is read.
+int encode_cache_head_map(CUtensorMap* map, const void* base, int64_t num_blocks,
+                          int32_t block_size, int32_t hkv, int32_t d) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (block_size != 16) return fail(PKV_E_UNSUPPORTED, "block_size must be 16");
+  const cuuint64_t row = static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(hkv);
+  cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(d / 64), static_cast<cuuint64_t>(hkv),
+                        static_cast<cuuint64_t>(num_blocks * 2)};
+  cuuint64_t strides[4] = {row, 128, static_cast<cuuint64_t>(d) * 2, row * 8};
+  cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(d / 64), 1, 2};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled (head) failed (%d)", int(r));
+  return PKV_OK;
+}
+
 // The [T, H, D] query (token stride q_stride elements) as a 3-D tensor
 // (D, H, T), box = 64 dims x G heads x 128/G tokens, 128-byte swizzle: one box
 // is the 128-row (token, head-in-group) tile of the prefill kernel.
@@ -233,22 +281,26 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
   const int group = num_heads / num_kv_heads;
   if (num_kv_heads > 8 || group > 16 || (group & (group - 1)))
     return fail(PKV_E_UNSUPPORTED, "bf16 path supports num_kv_heads <= 8 and G in {1,2,4,8,16}");
-  CUtensorMap kmap, vmap;
-  int rc = encode_cache_map(&kmap, key_cache, num_blocks, block_size, num_kv_heads, head_dim);
+  CUtensorMap kblk, vblk;
+  int rc = encode_cache_block_map(&kblk, key_cache, num_blocks, block_size, num_kv_heads, head_dim);
   if (rc != PKV_OK) return rc;
-  rc = encode_cache_map(&vmap, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
+  rc = encode_cache_block_map(&vblk, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
   if (rc != PKV_OK) return rc;
   DecodeScratch ds;
   ds.counters = reinterpret_cast<int32_t*>(ws + wl.counters);
   ds.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   ds.part_o = reinterpret_cast<float*>(ws + wl.part_o);
   ds.num_slots = wl.slots;
-  cudaError_t e = launch_decode_bf16(a, kmap, vmap, ds, grid, st);
+  cudaError_t e = launch_decode_bf16(a, kblk, vblk, ds, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (max_query_len != 1) {
-    CUtensorMap qmap;
+    CUtensorMap qmap, kmap, vmap;
     rc = encode_query_map(&qmap, q, q_stride, num_tokens, num_heads, num_heads / num_kv_heads,
                           head_dim);
+    if (rc != PKV_OK) return rc;
+    rc = encode_cache_head_map(&kmap, key_cache, num_blocks, block_size, num_kv_heads, head_dim);
+    if (rc != PKV_OK) return rc;
+    rc = encode_cache_map(&vmap, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
     if (rc != PKV_OK) return rc;
     e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -186,16 +186,10 @@ __global__ void __launch_bounds__(288, 1)
               alive = 0;
             } else {
               mbar_arrive_expect_tx(&full_bar[stage], p.stage_bytes);
+              // one box per cache: the whole block, landing [head][dim half][token]
               uint8_t* kdst = smem + stage * p.stage_bytes;
-              uint8_t* vdst = kdst + kv_region;
-              for (int h = 0; h < hkv; ++h) {
-#pragma unroll
-                for (int dh = 0; dh < NDH; ++dh) {
-                  const uint32_t off = (h * NDH + dh) * kBox;
-                  tma_load_3d(kdst + off, &kmap, dh * 64, h, pb * 16, &full_bar[stage]);
-                  tma_load_3d(vdst + off, &vmap, dh * 64, h, pb * 16, &full_bar[stage]);
-                }
-              }
+              tma_load_4d(kdst, &kmap, 0, pb * 16, 0, 0, &full_bar[stage]);
+              tma_load_4d(kdst + kv_region, &vmap, 0, pb * 16, 0, 0, &full_bar[stage]);
             }
           }
           if (!__shfl_sync(0xffffffffu, alive, 0)) return;

@@ -9,9 +9,11 @@
 //
 // Tiling.  A tile is 128 rows = 128/G query tokens x the G query heads of one
 // KV head, so each K/V tile serves all G heads (GQA packing).  Keys come in
-// tiles of 128 = eight 16-token paged blocks; each block is one TMA box per
-// 64-dim half, landing 128-byte swizzled so that the 8 boxes form one
-// [128 keys x 64 dims] operand region.  Per key tile j:
+// tiles of 128 = eight 16-token paged blocks.  A block of K is one TMA box
+// that lands as [token half][dim half][8 keys][128 B], 128-byte swizzled, so
+// the K operand is K-major with groups of 8 keys D/64 KiB apart; a block of V
+// is one box per 64-dim half, and the 8 boxes of a half form one
+// [128 keys x 64 dims] MN-major operand region.  Per key tile j:
 //   S_j = Q K_j^T   tcgen05.mma M=128 N=128 K=D from shared memory, fp32 in
 //                   tensor memory (two S buffers)
 //   softmax        eight warps, two per 32-lane quadrant of tensor memory:
@@ -81,7 +83,7 @@ enum Bar {
   kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2,
   kVFull0, kVFull1, kVEmpty0, kVEmpty1,
   kSFull0, kSFull1, kSFree0, kSFree1,
-  kPFull, kODone, kXchg,
+  kPFull0, kPFull1, kODone, kOFinal, kXchg,
   kNumBars
 };
 static_assert(kKFull0 + kKStages == kKEmpty0 && kKEmpty0 + kKStages == kVFull0,
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int b = 0; b < kNumBars; ++b) {
       uint32_t n = 1;
-      if (b == kPFull || b == kXchg) n = kSoftmaxWarps;
+      if (b == kPFull0 || b == kPFull1 || b == kXchg) n = kSoftmaxWarps;
       if ((b >= kKEmpty0 && b < kKEmpty0 + kKStages) || (b >= kVEmpty0 && b < kVEmpty0 + kVStages))
         n = C;  // released by the MMAs of every cluster member
       mbar_init(&bars[b], n);
@@ -283,19 +285,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&bars[full0 + st], NDH * kBox * nvalid);
           uint8_t* dst = ring + st * L::kHalf;
-          // box i = k * NDH + dh goes out from member i % C to all members
+          if (is_k) {
+            // K: one box per block, [token half][dim half][8 keys][128 B];
+            // block k goes out from member k % C to all members
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            if (k < nvalid)
-              for (int dh = 0; dh < NDH; ++dh) {
-                if (C == 1) {
-                  tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
-                              &bars[full0 + st]);
-                } else if ((k * NDH + dh) % C == rank) {
-                  tma_load_3d_multicast(dst + dh * kRegion + k * kBox, map, dh * 64, t.h,
-                                        phys[k] * 16, &bars[full0 + st], kMask);
-                }
+            for (int k = 0; k < 8; ++k)
+              if (k < nvalid && (C == 1 || k % C == rank)) {
+                uint8_t* d = dst + k * NDH * kBox;
+                if (C == 1)
+                  tma_load_5d(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st]);
+                else
+                  tma_load_5d_multicast(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st],
+                                        kMask);
               }
+          } else {
+            // V: [dim half][128 keys][128 B], one box per block and dim half;
+            // box i = k * NDH + dh goes out from member i % C
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (k < nvalid)
+                for (int dh = 0; dh < NDH; ++dh) {
+                  if (C == 1) {
+                    tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
+                                &bars[full0 + st]);
+                  } else if ((k * NDH + dh) % C == rank) {
+                    tma_load_3d_multicast(dst + dh * kRegion + k * kBox, map, dh * 64, t.h,
+                                          phys[k] * 16, &bars[full0 + st], kMask);
+                  }
+                }
+          }
           ++count;
         }
         if (!ok) break;
@@ -317,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // descriptors are built once; a stage or k-step only adds its byte
       // offset >> 4 to the start-address field
       const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
-      const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      // K stage: groups of 8 keys every NDH KiB, dim half dh at +dh KiB
+      const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + L::kK), 16, NDH * 1024);
       uint32_t q_count = 0, k_count = 0, s_count = 0;
       bool ok = true;
       for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
@@ -337,8 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_s = tmem + kColS + b * kKeys;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = ((kk >> 2) * kRegion + (kk & 3) * 32) >> 4;
-            tc_mma_ss(d_s, q_desc + off, kd + off, idesc_s, kk > 0);
+            const uint64_t q_off = ((kk >> 2) * kRegion + (kk & 3) * 32) >> 4;
+            const uint64_t k_off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            tc_mma_ss(d_s, q_desc + q_off, kd + k_off, idesc_s, kk > 0);
           }
           tc_commit(&bars[kSFull0 + b]);
           if (C == 1) tc_commit(&bars[kKEmpty0 + ks]);
@@ -354,14 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
       const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + L::kV), kRegion, 1024);
-      uint32_t v_count = 0, s_count = 0, p_count = 0;
+      uint32_t v_count = 0, s_count = 0;
       bool ok = true;
       for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
         const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
         for (int j = 0; j < t.nkt && ok; ++j) {
           const int vs = v_count % kVStages;
           const int b = s_count & 1;
-          ok = mbar_wait_or_abort(&bars[kPFull], p_count & 1, p.err, abort_flag) &&
+          // P of S buffer b: one barrier per buffer, so that a softmax warp
+          // already done with the next key tile (it only needs the PV before
+          // this one) cannot complete this tile's phase for a slower warp
+          ok = mbar_wait_or_abort(&bars[kPFull0 + b], (s_count >> 1) & 1, p.err, abort_flag) &&
                mbar_wait_or_abort(&bars[kVFull0 + vs], (v_count / kVStages) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -377,12 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&bars[kODone]);
+          if (j == t.nkt - 1) tc_commit(&bars[kOFinal]);
           tc_commit(&bars[kSFree0 + b]);
           if (C == 1) tc_commit(&bars[kVEmpty0 + vs]);
           else tc_commit_multicast(&bars[kVEmpty0 + vs], kMask);
           ++v_count;
           ++s_count;
-          ++p_count;
         }
       }
     }
@@ -496,11 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++v_count;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kPFull]);
+        if (lane == 0) mbar_arrive(&bars[kPFull0 + b]);
       }
       if (!ok) break;
       // ---- epilogue: merge the two halves, O / l -> out ----
-      if (!warp_wait(&bars[kODone], o_count & 1, p.err, abort_flag)) break;
+      // O is final once the tile's last PV is done.  That is waited for on a
+      // barrier with one phase per tile: o_done may still be two phases short
+      // here (only PV(n-3) is known complete), and a parity wait on it would
+      // then match the earlier phase of equal parity.
+      if (!warp_wait(&bars[kOFinal], tiles_done & 1, p.err, abort_flag)) break;
       ++o_count;
       tc_fence_after();
       float2* mine_x = xch + ((tiles_done & 1) * 2 + half) * 128;

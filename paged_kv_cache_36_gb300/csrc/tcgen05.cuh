@@ -196,6 +196,17 @@ __device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorM
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d_multicast(void* dst, const CUtensorMap* map, int32_t c0,
+                                                      int32_t c1, int32_t c2, int32_t c3,
+                                                      int32_t c4, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
 // Like tc_commit, but arrives on the mbarrier at `bar`'s offset in every CTA
 // of `mask`.
 __device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t mask) {

@@ -151,6 +151,9 @@ CASES = [
     (64, 8, 128, [100, 1], [3000, 5]),
     (16, 8, 128, [150], [17]),
     (32, 2, 128, [40, 1], [60, 9]),
+    # one query tile per request (single-CTA tiles) over long histories
+    (32, 8, 128, [32, 1, 17], [1500, 20, 3000]),
+    (8, 8, 64, [128, 1], [2000, 700]),
 ]
 
 
@@ -171,6 +174,43 @@ def test_random_varlen_bf16(case):
     b = Batch(kv, blocks, NB, qlens, ncs, q, H, torch.bfloat16).alloc_cache().fill_history()
     b.upload_metadata().write_new_tokens()
     compare(b.attention(), b.oracle(), b.qsl_host, torch.bfloat16)
+
+
+def _repeat_case(name, qlens, ncs, H=32, Hkv=8, D=128, reps=12):
+    seq = [a + b for a, b in zip(qlens, ncs)]
+    counts = [(s + 15) // 16 for s in seq]
+    NB = sum(counts) + 64
+    blocks = random_block_placement(NB, counts, name, "placement")
+    lengths = np.array(seq, np.int64)
+    offsets = np.concatenate([[0], np.cumsum(lengths)[:-1]]).astype(np.int64)
+    n = int(lengths.sum())
+    kv = KVHistory(randn_fp32((n, Hkv, D), name, "k", dtype=torch.bfloat16),
+                   randn_fp32((n, Hkv, D), name, "v", dtype=torch.bfloat16), lengths, offsets)
+    q = randn_fp32((sum(qlens), H, D), name, "q", dtype=torch.bfloat16)
+    b = Batch(kv, blocks, NB, qlens, ncs, q, H, torch.bfloat16).alloc_cache().fill_history()
+    b.upload_metadata().write_new_tokens()
+    ws = _pkv().new_workspace(b.R, H, D)
+    first = b.attention(ws).clone()
+    compare(first, b.oracle(), b.qsl_host, torch.bfloat16)
+    for _ in range(reps):
+        again = b.attention(ws)
+        assert torch.equal(again, first), "output changed between identical calls"
+
+
+def test_repeated_single_tile_requests_over_long_histories():
+    """96 requests of one query tile each (32 tokens, 4 query heads per KV
+    head) over 1000-3000 computed tokens: one CTA per tile, many key tiles.
+    Every call must match the oracle bit for bit with the first; the softmax
+    warps here can run two key tiles ahead of the PV products, which is what
+    the epilogue's wait must tolerate."""
+    R = 96
+    ncs = uniform_int(1000, 3000, R, "repeat1", "nc").tolist()
+    _repeat_case("repeat1", [32] * R, ncs)
+
+
+def test_repeated_long_chunk():
+    """The 512-token chunk at [1536, 2048) repeated: clustered K/V sharing."""
+    _repeat_case("repeat2", [512], [1536])
 
 
 def test_workspace_reuse_and_error_word():
