@@ -241,85 +241,107 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================ TMA producers ============================
     // warp 0 streams Q and K, warp 3 streams V.  They are separate warps so
     // that neither waits on the other's ring: two lanes of one warp would run
-    // converged, and K would stall whenever V waits for a free stage.
-    if (lane == 0) {
-      const bool is_k = warp == 0;
-      const int nst = is_k ? kKStages : kVStages;
-      const int full0 = is_k ? kKFull0 : kVFull0;
-      const int empty0 = is_k ? kKEmpty0 : kVEmpty0;
-      const CUtensorMap* map = is_k ? &kmap : &vmap;
-      uint8_t* ring = smem + (is_k ? L::kK : L::kV);
-      uint32_t q_uses = 0, count = 0;
-      for (int ct = cid; ct < total && !*abort_flag; ct += ncl) {
-        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
-        if (is_k) {
-          if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag))
-            break;
-          mbar_arrive_expect_tx(&bars[kQFull], L::kHalf);
-          for (int dh = 0; dh < NDH; ++dh)
-            tma_load_3d(smem + L::kQ + dh * kRegion, &qmap, dh * 64, t.h * G,
-                        static_cast<int32_t>(t.qs + t.u0), &bars[kQFull]);
-          ++q_uses;
+    // converged, and K would stall whenever V waits for a free stage.  The
+    // whole warp reads the block table, 32 entries per coalesced load and one
+    // batch ahead, so no key tile waits on a block-table read; lane 0 waits
+    // for free stages and issues the copies.
+    const bool is_k = warp == 0;
+    const int nst = is_k ? kKStages : kVStages;
+    const int full0 = is_k ? kKFull0 : kVFull0;
+    const int empty0 = is_k ? kKEmpty0 : kVEmpty0;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    uint8_t* ring = smem + (is_k ? L::kK : L::kV);
+    uint32_t q_uses = 0, count = 0;
+    bool ok = true;
+    for (int ct = cid; ct < total && ok; ct += ncl) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
+      const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
+      const int nblk = (t.nkeys + 15) / 16;
+      // block ids [batch, batch + 32) in `cur`, the next 32 in `nxt`
+      auto load_ids = [&](int first) -> int32_t {
+        const int b = first + lane;
+        int32_t v = b < nblk ? __ldg(row + b) : 0;
+        if (b < nblk && (v < 0 || v >= p.num_blocks)) {
+          if (is_k) atomicOr(p.err, PKV_ERR_BLOCK_ID);
+          v = p.num_blocks;  // out of the tensor: TMA fills zeros
         }
-        const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
-        const int nblk = (t.nkeys + 15) / 16;
-        bool ok = true;
-        for (int j = 0; j < t.nkt && ok; ++j) {
-          const int b0 = j * 8;
-          const int nvalid = min(8, nblk - b0);
-          int32_t phys[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            int32_t v = k < nvalid ? __ldg(row + b0 + k) : 0;
-            if (k < nvalid && (v < 0 || v >= p.num_blocks)) {
-              if (is_k) atomicOr(p.err, PKV_ERR_BLOCK_ID);
-              v = p.num_blocks;  // out of the tensor: TMA fills zeros
-            }
-            phys[k] = v;
+        return v;
+      };
+      int batch = 0;
+      int32_t cur = load_ids(0), nxt = load_ids(32);
+      if (is_k) {
+        if (lane == 0) {
+          if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag)) {
+            ok = false;
+          } else {
+            mbar_arrive_expect_tx(&bars[kQFull], L::kHalf);
+            for (int dh = 0; dh < NDH; ++dh)
+              tma_load_3d(smem + L::kQ + dh * kRegion, &qmap, dh * 64, t.h * G,
+                          static_cast<int32_t>(t.qs + t.u0), &bars[kQFull]);
           }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++q_uses;
+      }
+      for (int j = 0; j < t.nkt && ok; ++j) {
+        const int b0 = j * 8;
+        if (b0 >= batch + 32) {
+          batch += 32;
+          cur = nxt;
+          nxt = load_ids(batch + 32);
+        }
+        const int nvalid = min(8, nblk - b0);
+        int32_t phys[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) phys[k] = __shfl_sync(0xffffffffu, cur, (b0 - batch) + k);
+        if (lane == 0) {
           const int st = count % nst;
           const uint32_t n = count / nst;
           if (n > 0 && !mbar_wait_or_abort(&bars[empty0 + st], (n - 1) & 1, p.err, abort_flag)) {
             ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars[full0 + st], NDH * kBox * nvalid);
-          uint8_t* dst = ring + st * L::kHalf;
-          if (is_k) {
-            // K: one box per block, [token half][dim half][8 keys][128 B];
-            // block k goes out from member k % C to all members
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (k < nvalid && (C == 1 || k % C == rank)) {
-                uint8_t* d = dst + k * NDH * kBox;
-                if (C == 1)
-                  tma_load_5d(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st]);
-                else
-                  tma_load_5d_multicast(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st],
-                                        kMask);
-              }
           } else {
-            // V: [dim half][128 keys][128 B], one box per block and dim half;
-            // box i = k * NDH + dh goes out from member i % C
+            mbar_arrive_expect_tx(&bars[full0 + st], NDH * kBox * nvalid);
+            uint8_t* dst = ring + st * L::kHalf;
+            if (is_k) {
+              // K: one box per block, [token half][dim half][8 keys][128 B];
+              // block k goes out from member k % C to all members
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (k < nvalid)
-                for (int dh = 0; dh < NDH; ++dh) {
-                  if (C == 1) {
-                    tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
-                                &bars[full0 + st]);
-                  } else if ((k * NDH + dh) % C == rank) {
-                    tma_load_3d_multicast(dst + dh * kRegion + k * kBox, map, dh * 64, t.h,
-                                          phys[k] * 16, &bars[full0 + st], kMask);
-                  }
+              for (int k = 0; k < 8; ++k)
+                if (k < nvalid && (C == 1 || k % C == rank)) {
+                  uint8_t* d = dst + k * NDH * kBox;
+                  if (C == 1)
+                    tma_load_5d(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st]);
+                  else
+                    tma_load_5d_multicast(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st],
+                                          kMask);
                 }
+            } else {
+              // V: [dim half][128 keys][128 B], one box per block and dim half;
+              // box i = k * NDH + dh goes out from member i % C
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (k < nvalid)
+                  for (int dh = 0; dh < NDH; ++dh) {
+                    if (C == 1) {
+                      tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
+                                  &bars[full0 + st]);
+                    } else if ((k * NDH + dh) % C == rank) {
+                      tma_load_3d_multicast(dst + dh * kRegion + k * kBox, map, dh * 64, t.h,
+                                            phys[k] * 16, &bars[full0 + st], kMask);
+                    }
+                  }
+            }
           }
-          ++count;
         }
-        if (!ok) break;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ++count;
       }
-      // drain: every copy into this CTA's ring (and, in a cluster, every
-      // member's release of it) has landed before the CTA may exit
+    }
+    // drain: every copy into this CTA's ring (and, in a cluster, every
+    // member's release of it) has landed before the CTA may exit
+    if (lane == 0) {
       for (int st = 0; st < nst; ++st) {
         const uint32_t uses = count / nst + (static_cast<uint32_t>(st) < count % nst ? 1u : 0u);
         if (uses == 0) continue;
