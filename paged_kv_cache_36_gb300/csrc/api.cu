@@ -80,31 +80,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D view [num_blocks * block_size tokens][num_kv_heads][head_dim] of one
-// cache, box = 64 dims x 1 head x 16 tokens, 128-byte swizzle.
-int encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int32_t block_size,
-                     int32_t hkv, int32_t d) {
-  auto fn = encode_fn();
-  if (!fn) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
-                        static_cast<cuuint64_t>(num_blocks * block_size)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(hkv)};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(block_size)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(PKV_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
-  return PKV_OK;
-}
-
 // One paged block of one cache, all heads, as a single box: the 4-D view
 // (64 dims, num_blocks * block_size tokens, head_dim / 64 halves, num_kv_heads)
 // with strides (2 B, row, 128 B, head_dim * 2 B) and box (64, block_size,
 // head_dim / 64, num_kv_heads).  The box lands as [head][half][token][128 B],
-// 128-byte swizzled, so one copy fetches what 2 * num_kv_heads boxes of
-// encode_cache_map would.
+// 128-byte swizzled: one copy per block and cache instead of one per head and
+// 64-dim half.
 int encode_cache_block_map(CUtensorMap* map, const void* base, int64_t num_blocks,
                            int32_t block_size, int32_t hkv, int32_t d) {
   auto fn = encode_fn();
@@ -300,7 +281,7 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
     if (rc != PKV_OK) return rc;
     rc = encode_cache_head_map(&kmap, key_cache, num_blocks, block_size, num_kv_heads, head_dim);
     if (rc != PKV_OK) return rc;
-    rc = encode_cache_map(&vmap, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
+    rc = encode_cache_head_map(&vmap, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
     if (rc != PKV_OK) return rc;
     e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -9,25 +9,25 @@
 //
 // Tiling.  A tile is 128 rows = 128/G query tokens x the G query heads of one
 // KV head, so each K/V tile serves all G heads (GQA packing).  Keys come in
-// tiles of 128 = eight 16-token paged blocks.  A block of K is one TMA box
-// that lands as [token half][dim half][8 keys][128 B], 128-byte swizzled, so
-// the K operand is K-major with groups of 8 keys D/64 KiB apart; a block of V
-// is one box per 64-dim half, and the 8 boxes of a half form one
-// [128 keys x 64 dims] MN-major operand region.  Per key tile j:
+// tiles of 128 = eight 16-token paged blocks.  A block of K or V (one head)
+// is one TMA box that lands as [token half][dim half][8 keys][128 B],
+// 128-byte swizzled: read K-major this is the K operand (groups of 8 keys
+// D/64 KiB apart), read MN-major the V operand (64-dim atoms 1 KiB apart,
+// groups of 8 keys D/64 KiB apart).  Per key tile j:
 //   S_j = Q K_j^T   tcgen05.mma M=128 N=128 K=D from shared memory, fp32 in
-//                   tensor memory (two S buffers)
+//                   tensor memory (three S buffers)
 //   softmax        eight warps, two per 32-lane quadrant of tensor memory:
-//                   warp half h owns keys [64h, 64h + 64) of every tile, keeps
-//                   its own running max and sum, and writes its P (bf16) back
+//                   warp half h reads keys [64h, 64h + 64) of every tile; the
+//                   two warps of a quadrant exchange their row maxima, so both
+//                   use one running max, and each writes its P (bf16) back
 //                   over the S columns it has just read
-//   O_h += P_h V_h tcgen05.mma with A = P from tensor memory and B = V rows
-//                   [64h, 64h + 64) read MN-major from shared memory
-// The two halves are two independent online softmaxes over disjoint key sets;
-// the epilogue merges them exactly: with M = max(m_0, m_1) and w_h =
-// 2^(m_h - M), out = (w_0 O_0 + w_1 O_1) / (w_0 l_0 + w_1 l_1).  A running
-// max is only moved (and its O, l rescaled) when it would grow by more than
-// 2^8; otherwise the stale max keeps P <= 256, the same arithmetic with a
-// different reference point.
+//   O += P_j V_j   tcgen05.mma with A = P from tensor memory and B = V read
+//                   MN-major from shared memory, one fp32 accumulator
+// A running max is only moved (and O, l rescaled) when it would grow by more
+// than 2^8; otherwise the stale max keeps P <= 256, the same arithmetic with a
+// different reference point.  With three S buffers, QK of key tile j + 3
+// waits only for PV of key tile j, so the tensor core runs ahead of the
+// softmax instead of alternating with it.
 //
 // Warp roles (12 warps): warp 0 streams Q and K (3-stage ring), warp 3
 // streams V (2-stage ring); warp 1 owns the tensor memory and issues QK^T;
@@ -67,13 +67,14 @@ constexpr uint32_t kRegion = 16384;  // 128 rows x 128 bytes
 constexpr uint32_t kBox = 2048;      // 16 rows x 128 bytes
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
+constexpr int kSBufs = 3;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (4 + kSoftmaxWarps) * 32;
-// tensor memory: S/P buffers 0 and 1 (128 fp32 columns each; a warp half's P
-// overwrites the first 32 of its own 64 S columns), O_0 and O_1 (D columns)
+// tensor memory: three S/P buffers of 128 fp32 columns (a softmax warp's P
+// overwrites the first 32 of its own 64 S columns) and the O accumulator
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = kSBufs * kKeys;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr size_t kPrefillSmemLimit = 232448;  // 227 KiB per CTA
 constexpr int kMaxDevices = 64;
@@ -82,14 +83,19 @@ enum Bar {
   kQFull, kQEmpty,
   kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2,
   kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-  kSFull0, kSFull1, kSFree0, kSFree1,
-  kPFull0, kPFull1, kODone, kOFinal, kXchg,
+  kSFull0, kSFull1, kSFull2, kSFree0, kSFree1, kSFree2,
+  kPFull0, kPFull1, kPFull2, kODone0, kODone1, kODone2,
+  kOFinal, kPair0, kPair1, kPair2, kPair3,
   kNumBars
 };
 static_assert(kKFull0 + kKStages == kKEmpty0 && kKEmpty0 + kKStages == kVFull0,
               "one full and one empty barrier per K stage");
 static_assert(kVFull0 + kVStages == kVEmpty0 && kVEmpty0 + kVStages == kSFull0,
               "one full and one empty barrier per V stage");
+static_assert(kSFull0 + kSBufs == kSFree0 && kSFree0 + kSBufs == kPFull0 &&
+                  kPFull0 + kSBufs == kODone0 && kODone0 + kSBufs == kOFinal,
+              "S-full, S-free, P-full and O-done: one barrier per S buffer");
+static_assert(kColO + 128 <= kTmemCols, "S buffers and O fit in tensor memory");
 
 struct PrefillParams {
   const int32_t* block_table;
@@ -124,8 +130,8 @@ struct Layout {
   static constexpr uint32_t kK = kQ + kHalf;
   static constexpr uint32_t kV = kK + kKStages * kHalf;
   static constexpr uint32_t kBars = kV + kVStages * kHalf;
-  static constexpr uint32_t kXch = kBars + 8 * kNumBars;      // [2 parity][2 half][128 rows] x (m, l)
-  static constexpr uint32_t kMisc = kXch + 2 * 2 * 128 * 8;   // tmem slot, abort flag
+  static constexpr uint32_t kXch = kBars + 8 * kNumBars;      // [2 parity][2 half][128 rows] floats
+  static constexpr uint32_t kMisc = kXch + 2 * 2 * 128 * 4;   // tmem slot, abort flag
   static constexpr uint32_t kPrefix = kMisc + 16;
 };
 
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  float2* xch = reinterpret_cast<float2*>(smem + L::kXch);
+  float* xch = reinterpret_cast<float*>(smem + L::kXch);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kPrefix);
@@ -195,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int b = 0; b < kNumBars; ++b) {
       uint32_t n = 1;
-      if (b == kPFull0 || b == kPFull1 || b == kXchg) n = kSoftmaxWarps;
+      if (b >= kPFull0 && b < kPFull0 + kSBufs) n = kSoftmaxWarps;
+      if (b >= kPair0 && b < kPair0 + 4) n = 2;  // the two warps sharing a quadrant
       if ((b >= kKEmpty0 && b < kKEmpty0 + kKStages) || (b >= kVEmpty0 && b < kVEmpty0 + kVStages))
         n = C;  // released by the MMAs of every cluster member
       mbar_init(&bars[b], n);
@@ -303,36 +310,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
           } else {
             mbar_arrive_expect_tx(&bars[full0 + st], NDH * kBox * nvalid);
+            // one box per block, landing [token half][dim half][8 keys][128 B];
+            // block k goes out from member k % C to all members
             uint8_t* dst = ring + st * L::kHalf;
-            if (is_k) {
-              // K: one box per block, [token half][dim half][8 keys][128 B];
-              // block k goes out from member k % C to all members
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                if (k < nvalid && (C == 1 || k % C == rank)) {
-                  uint8_t* d = dst + k * NDH * kBox;
-                  if (C == 1)
-                    tma_load_5d(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st]);
-                  else
-                    tma_load_5d_multicast(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st],
-                                          kMask);
-                }
-            } else {
-              // V: [dim half][128 keys][128 B], one box per block and dim half;
-              // box i = k * NDH + dh goes out from member i % C
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                if (k < nvalid)
-                  for (int dh = 0; dh < NDH; ++dh) {
-                    if (C == 1) {
-                      tma_load_3d(dst + dh * kRegion + k * kBox, map, dh * 64, t.h, phys[k] * 16,
-                                  &bars[full0 + st]);
-                    } else if ((k * NDH + dh) % C == rank) {
-                      tma_load_3d_multicast(dst + dh * kRegion + k * kBox, map, dh * 64, t.h,
-                                            phys[k] * 16, &bars[full0 + st], kMask);
-                    }
-                  }
-            }
+            for (int k = 0; k < 8; ++k)
+              if (k < nvalid && (C == 1 || k % C == rank)) {
+                uint8_t* d = dst + k * NDH * kBox;
+                if (C == 1)
+                  tma_load_5d(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st]);
+                else
+                  tma_load_5d_multicast(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st],
+                                        kMask);
+              }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -367,11 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++q_count;
         for (int j = 0; j < t.nkt && ok; ++j) {
           const int ks = k_count % kKStages;
-          const int b = s_count & 1;
+          const int b = s_count % kSBufs;
+          const uint32_t use = s_count / kSBufs;
           ok = mbar_wait_or_abort(&bars[kKFull0 + ks], (k_count / kKStages) & 1, p.err, abort_flag);
-          // S/P buffer b is free once PV of the tile that last used it is done
-          if (ok && (s_count >> 1) > 0)
-            ok = mbar_wait_or_abort(&bars[kSFree0 + b], ((s_count >> 1) - 1) & 1, p.err, abort_flag);
+          // S/P buffer b is free once PV of the key tile that last used it is done
+          if (ok && use > 0)
+            ok = mbar_wait_or_abort(&bars[kSFree0 + b], (use - 1) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd = k_desc0 + ((ks * L::kHalf) >> 4);
@@ -395,33 +386,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================ PV issuer ============================
     if (lane == 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
-      const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + L::kV), kRegion, 1024);
+      // V stage, MN-major: the two 64-dim atoms of a group of 8 keys 1 KiB
+      // apart, groups of 8 keys NDH KiB apart
+      const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + L::kV), 1024, NDH * 1024);
       uint32_t v_count = 0, s_count = 0;
       bool ok = true;
       for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
         const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
         for (int j = 0; j < t.nkt && ok; ++j) {
           const int vs = v_count % kVStages;
-          const int b = s_count & 1;
+          const int b = s_count % kSBufs;
+          const uint32_t use = s_count / kSBufs;
           // P of S buffer b: one barrier per buffer, so that a softmax warp
-          // already done with the next key tile (it only needs the PV before
-          // this one) cannot complete this tile's phase for a slower warp
-          ok = mbar_wait_or_abort(&bars[kPFull0 + b], (s_count >> 1) & 1, p.err, abort_flag) &&
+          // already done with a later key tile cannot complete this tile's
+          // phase for a slower warp
+          ok = mbar_wait_or_abort(&bars[kPFull0 + b], use & 1, p.err, abort_flag) &&
                mbar_wait_or_abort(&bars[kVFull0 + vs], (v_count / kVStages) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t vd = v_desc0 + ((vs * L::kHalf) >> 4);
           const uint32_t a_p = tmem + kColS + b * kKeys;
+          // O += P V over the 128 keys: P columns hold the keys of each warp
+          // half in their first 32 (bf16 pairs), V rows [64 half, 64 half + 64)
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            const uint32_t d_o = tmem + kColO + half * D;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc_mma_ts(d_o, a_p + half * 64 + kk * 8,
-                        vd + (((half * 64 + kk * 16) * 128) >> 4), idesc_o,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_ts(tmem + kColO, a_p + half * 64 + kk * 8,
+                        vd + ((((half * 64 + kk * 16) / 8) * NDH * 1024) >> 4), idesc_o,
+                        (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&bars[kODone]);
+          tc_commit(&bars[kODone0 + b]);
           if (j == t.nkt - 1) tc_commit(&bars[kOFinal]);
           tc_commit(&bars[kSFree0 + b]);
           if (C == 1) tc_commit(&bars[kVEmpty0 + vs]);
@@ -433,13 +428,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ============================ softmax warps ============================
+    // Two warps share each 32-lane quadrant of tensor memory (the same 128/4
+    // rows): warp half h reads S columns [64 h, 64 h + 64).  They agree on the
+    // row maximum every key tile through a small exchange, so one O serves the
+    // whole row; each warp keeps the partial sum l of its own columns and
+    // rescales its half of O's columns.
     const int quad = warp & 3;
     const int half = (warp - 4) >> 2;    // keys [64 half, 64 half + 64) of each tile
     const int row = quad * 32 + lane;    // tile row = tensor-memory lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t o_cols = lane_addr + kColO + half * D;
+    const uint32_t o_cols = lane_addr + kColO + half * (D / 2);
     const float sl2 = p.scale_log2;
-    uint32_t s_count = 0, v_count = 0, o_count = 0, tiles_done = 0;
+    uint64_t* pair_bar = &bars[kPair0 + quad];
+    uint32_t s_count = 0, v_count = 0, pair_uses = 0, tiles_done = 0;
+    // row value exchanged with the partner warp; returns the partner's value
+    auto exchange = [&](float mine) -> float {
+      float* slot = xch + (pair_uses & 1) * 256;
+      slot[half * 128 + row] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pair_bar);
+      const bool done = warp_wait(pair_bar, pair_uses & 1, p.err, abort_flag);
+      ++pair_uses;
+      return done ? slot[(half ^ 1) * 128 + row] : mine;
+    };
     for (int ct = cid; ct < total; ct += ncl) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
@@ -450,8 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < t.nkt && ok; ++j) {
-        const int b = s_count & 1;
-        if (!warp_wait(&bars[kSFull0 + b], (s_count >> 1) & 1, p.err, abort_flag)) {
+        const uint32_t gs = s_count;  // this key tile's index in the CTA's sequence
+        const int b = gs % kSBufs;
+        if (!warp_wait(&bars[kSFull0 + b], (gs / kSBufs) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -475,23 +487,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+        const float m_mine = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+        const float mx = fmaxf(m_mine, exchange(m_mine));  // row max of the key tile
         if (j == 0) {
-          m_used = mx;  // may be -inf when this half sees no key yet
+          m_used = mx;  // finite: key 0 is visible to every row
         } else {
-          const bool mine = mx > m_used + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, mine)) {
-            // O must hold PV of the previous tile before it is rescaled
-            if (!warp_wait(&bars[kODone], o_count & 1, p.err, abort_flag)) {
+          // both warps of the quadrant see the same mx and m_used, so they
+          // take the same decision for every row
+          const bool grow = mx > m_used + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, grow)) {
+            // O must hold PV of the previous key tile before it is rescaled;
+            // o_done has one barrier per S buffer because the softmax may run
+            // two key tiles ahead of the PV products
+            const uint32_t prev = gs - 1;
+            if (!warp_wait(&bars[kODone0 + prev % kSBufs], (prev / kSBufs) & 1, p.err, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const float alpha = mine ? exp2_approx(m_used - mx) : 1.f;
-            if (mine) m_used = mx;
+            const float alpha = grow ? exp2_approx(m_used - mx) : 1.f;
+            if (grow) m_used = mx;
             l *= alpha;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
               uint32_t r32[32];
               tmem_ld32(o_cols + c * 32, r32);
               tmem_wait_ld();
@@ -503,10 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
         }
-        if (j > 0) ++o_count;  // PV of tile j-1 is the o_done phase this tile may wait on
         // P = 2^(s * scale_log2 - m_used) as bf16 pairs over the first 32 of
-        // this half's S columns (a row with no visible key yet gets P = 0)
-        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+        // this warp's 64 S columns
+        const float neg_m = -m_used;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t w[32];
 #pragma unroll
@@ -522,19 +539,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         // keys past the cluster's last row were not loaded: zero their V rows
         // so that 0 * (stale) stays 0
         if (j == t.nkt - 1 && j * kKeys + kKeys > t.nkeys) {
+          // The stage's previous tile (V of key tile gs - 2) may still be in
+          // use: this warp can be two key tiles ahead of the PV products.
+          // Wait for its release first (PV(gs - 4) is known complete, so that
+          // parity is unambiguous), then for this tile's copies.
           const int vs = v_count % kVStages;
-          if (!warp_wait(&bars[kVFull0 + vs], (v_count / kVStages) & 1, p.err, abort_flag)) {
+          const uint32_t round = v_count / kVStages;
+          if ((round > 0 &&
+               !warp_wait(&bars[kVEmpty0 + vs], (round - 1) & 1, p.err, abort_flag)) ||
+              !warp_wait(&bars[kVFull0 + vs], round & 1, p.err, abort_flag)) {
             ok = false;
             break;
           }
           const int key = j * kKeys + half * 64 + (quad & 1) * 32 + lane;
           if (quad < 2 && key >= t.nkeys) {
-            uint8_t* vrow = smem + L::kV + vs * L::kHalf + (key - j * kKeys) * 128;
+            const int k = key - j * kKeys;  // row of key k, dim half dh: group k / 8
+            uint8_t* vrow = smem + L::kV + vs * L::kHalf + (k / 8) * NDH * 1024 + (k % 8) * 128;
 #pragma unroll
             for (int dh = 0; dh < NDH; ++dh)
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(vrow + dh * kRegion + c * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(vrow + dh * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
@@ -544,50 +569,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kPFull0 + b]);
       }
       if (!ok) break;
-      // ---- epilogue: merge the two halves, O / l -> out ----
-      // O is final once the tile's last PV is done.  That is waited for on a
-      // barrier with one phase per tile: o_done may still be two phases short
-      // here (only PV(n-3) is known complete), and a parity wait on it would
-      // then match the earlier phase of equal parity.
+      // ---- epilogue: O / (l_0 + l_1) -> out ----
+      // O is final once the tile's last PV is done, waited for on a barrier
+      // with one phase per tile
       if (!warp_wait(&bars[kOFinal], tiles_done & 1, p.err, abort_flag)) break;
-      ++o_count;
-      tc_fence_after();
-      float2* mine_x = xch + ((tiles_done & 1) * 2 + half) * 128;
-      float2* other_x = xch + ((tiles_done & 1) * 2 + (half ^ 1)) * 128;
-      mine_x[row] = make_float2(m_used, l);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kXchg]);
-      if (!warp_wait(&bars[kXchg], tiles_done & 1, p.err, abort_flag)) break;
       ++tiles_done;
-      const float2 o = other_x[row];
-      const float m0 = half == 0 ? m_used : o.x, l0 = half == 0 ? l : o.y;
-      const float m1 = half == 0 ? o.x : m_used, l1 = half == 0 ? o.y : l;
-      const float mm = fmaxf(m0, m1);  // finite: key 0 is visible to every row
-      const float w0 = exp2_approx(m0 - mm), w1 = exp2_approx(m1 - mm);
-      const float inv = 1.f / (w0 * l0 + w1 * l1);
-      const float c0 = w0 * inv, c1 = w1 * inv;
+      tc_fence_after();
+      const float inv = 1.f / (l + exchange(l));
       __nv_bfloat16* orow =
           p.out + (t.qs + u) * p.out_stride + static_cast<int64_t>(t.h * G + row % G) * D;
       // this warp writes output dims [half * D/2, half * D/2 + D/2)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         const uint32_t col = half * (D / 2) + c * 32;
-        uint32_t r0[32], r1[32];
+        uint32_t r0[32];
         tmem_ld32(lane_addr + kColO + col, r0);
-        tmem_ld32(lane_addr + kColO + D + col, r1);
         tmem_wait_ld();
         if (valid_row && t.store) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              f[e] = __uint_as_float(r0[q4 * 8 + e]) * c0 + __uint_as_float(r1[q4 * 8 + e]) * c1;
             uint4 v;
-            v.x = pack_bf16(f[0], f[1]);
-            v.y = pack_bf16(f[2], f[3]);
-            v.z = pack_bf16(f[4], f[5]);
-            v.w = pack_bf16(f[6], f[7]);
+            v.x = pack_bf16(__uint_as_float(r0[q4 * 8 + 0]) * inv, __uint_as_float(r0[q4 * 8 + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(r0[q4 * 8 + 2]) * inv, __uint_as_float(r0[q4 * 8 + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(r0[q4 * 8 + 4]) * inv, __uint_as_float(r0[q4 * 8 + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(r0[q4 * 8 + 6]) * inv, __uint_as_float(r0[q4 * 8 + 7]) * inv);
             *reinterpret_cast<uint4*>(orow + col + q4 * 8) = v;
           }
         }
