@@ -50,6 +50,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged-attn decode HBM GB/s (% of peak); mixed-batch attention tokens/s/layer"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+CHUNK_COPIES = 20
 
 
 # ---------------------------------------------------------------------------
@@ -263,10 +264,69 @@ def build_mixed_step(pkv, device):
     vf[s] = cfg.kv.value[hr].to(device)
     step = DeviceStep(pkv, kc, vc, cfg.q, torch.cat(knew), torch.cat(vnew), cfg.blocks,
                       cfg.query_len, cfg.num_computed, cfg.num_heads, device)
-    # the prefill chunk alone, to time the prefill kernel on its own
-    chunk = DeviceStep(pkv, kc, vc, cfg.q[:int(cfg.query_len[0])], knew[0], vnew[0], cfg.blocks[:1],
-                       cfg.query_len[:1], cfg.num_computed[:1], cfg.num_heads, device)
-    return cfg, step, chunk
+    return cfg, step
+
+
+def build_prefill_chunks(pkv, device, copies=CHUNK_COPIES, pool_blocks=4096):
+    """The mixed step's 512-token prefill chunk at [1536, 2048) alone, in its
+    own 4096-block cache: `copies` placements of the request's 128 blocks on
+    disjoint random blocks (8.4 MB of K/V each, 168 MB for 20 against a
+    129 MB L2), so consecutive calls do not find the previous call's K/V in
+    L2."""
+    from workloads import configs
+    from workloads.generators import random_block_placement
+    cfg = configs.mixed_chunked_step()
+    nc, ql = int(cfg.num_computed[0]), int(cfg.query_len[0])
+    n0 = (nc + ql + 15) // 16
+    placements = random_block_placement(pool_blocks, [n0] * copies, cfg.name, "chunk copies")
+    shape = (pool_blocks, 16, cfg.num_kv_heads, cfg.head_dim)
+    kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    kf, vf = kc.view(-1, cfg.num_kv_heads, cfg.head_dim), vc.view(-1, cfg.num_kv_heads, cfg.head_dim)
+    o = int(cfg.kv.offsets[0])
+    # the history and the chunk's own new keys (as reshape_and_cache leaves them)
+    hist_k = cfg.kv.key[o:o + nc + ql].to(device)
+    hist_v = cfg.kv.value[o:o + nc + ql].to(device)
+    p = np.arange(nc + ql)
+    chunks = []
+    for blk in placements:
+        b = blk.astype(np.int64)
+        s = torch.from_numpy(b[p // 16] * 16 + p % 16).to(device)
+        kf[s] = hist_k
+        vf[s] = hist_v
+        chunks.append(DeviceStep(pkv, kc, vc, cfg.q[:ql], cfg.kv.key[o + nc:o + nc + ql],
+                                 cfg.kv.value[o + nc:o + nc + ql], [blk], cfg.query_len[:1],
+                                 cfg.num_computed[:1], cfg.num_heads, device))
+    return chunks
+
+
+def graph_time(calls, reps=5):
+    """Captures calls (a list of callables) in one CUDA graph and returns the
+    median over `reps` replays of the replay time per call, in ms: GPU time
+    without the host's per-call launch work."""
+    cur = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        for c in calls[:3]:
+            c()
+    cur.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        g.replay()
+        b.record(cur)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / len(calls))
+    del g
+    return statistics.median(times)
 
 
 def time_loop(fn_list, steps, stream, per_call=None):
@@ -389,6 +449,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="primary timed steps only (no e2e, secondary or CPU legs), for ncu")
+    ap.add_argument("--profile-prefill", action="store_true",
+                    help="only --steps calls of the 512-token chunk (rotating placements), for ncu")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -412,6 +474,14 @@ def main():
         dist.init_process_group("nccl", device_id=device)
     hbm_peak, bf16_peak, bf16_sust, peak_kind = peaks()
     stream = torch.cuda.current_stream()
+    if args.profile_prefill:
+        chunks = build_prefill_chunks(pkv, device)
+        for i in range(args.warmup + args.steps):
+            chunks[i % len(chunks)].attn()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_prefill_calls": args.warmup + args.steps,
+                          "error_word": pkv.read_error_word(chunks[0].ws)}))
+        return
 
     cfg, steps = build_decode_steps(pkv, device)
     for i in range(args.warmup):
@@ -477,20 +547,18 @@ def main():
     # ---- secondary: the mixed chunked-prefill step ----
     secondary = None
     if not args.no_secondary:
-        mcfg, mstep, chunk = build_mixed_step(pkv, device)
-        for _ in range(args.warmup):
+        mcfg, mstep = build_mixed_step(pkv, device)
+        chunks = build_prefill_chunks(pkv, device)
+        for i in range(args.warmup):
             mstep.step()
-            chunk.attn()
+            chunks[i % len(chunks)].attn()
         n2 = max(20, min(args.steps // 10, 300))
         tot, _ = time_loop([mstep], n2, stream)
-        cstart, cend = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        cstart.record(stream)
-        for _ in range(n2):
-            chunk.attn()
-        cend.record(stream)
-        cend.synchronize()
-        chunk_ms = cstart.elapsed_time(cend) / n2
         mixed_ms = tot / n2
+        # one call per placement, each a decode launch with no rows plus the
+        # prefill kernel (launched as its programmatic dependent)
+        chunk_ms = graph_time([c.attn for c in chunks] * 5)
+        chunk_tflops = mstep.prefill_flops / (chunk_ms * 1e-3) / 1e12
         secondary = {
             "metric": "mixed-batch attention tokens/s/layer",
             "value": mstep.T * world / (mixed_ms * 1e-3), "unit": "tokens/s/layer",
@@ -498,11 +566,20 @@ def main():
             "workload": "512-token prefill chunk at [1536,2048) + 256 decodes (ctx U[256,8192]), "
                         "Llama-3-8B heads, 131072-block pool",
             "prefill_chunk_ms": chunk_ms,
-            "prefill_tflops": mstep.prefill_flops / (chunk_ms * 1e-3) / 1e12,
-            "prefill_frac_of_bf16_peak": mstep.prefill_flops / (chunk_ms * 1e-3) / 1e12 / bf16_peak,
+            "prefill_tflops": chunk_tflops,
+            "prefill_roofline": {
+                "kernel": "prefill_tcgen05_kernel", "bound": "tensor", "achieved": chunk_tflops,
+                "peak": bf16_peak, "unit": "TFLOP/s", "frac": chunk_tflops / bf16_peak,
+                "peak_kind": peak_kind, "algorithmic_flops_per_launch": mstep.prefill_flops,
+                "avg_launch_ms": chunk_ms,
+                "timing": f"CUDA graph of {5 * CHUNK_COPIES} calls rotating over {CHUNK_COPIES} "
+                          f"disjoint placements of the chunk in a 4096-block cache (168 MB of "
+                          f"K/V > L2); per call: the decode launch (no rows) and the prefill "
+                          f"kernel",
+            },
             "decode_gbs_in_step": None,
         }
-        del mstep, chunk
+        del mstep, chunks
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
