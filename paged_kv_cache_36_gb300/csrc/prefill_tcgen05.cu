@@ -111,7 +111,12 @@ struct PrefillParams {
   int32_t group;
   float scale_log2;
   uint32_t* err;
+  int32_t cache_reqs;  // query_start_loc and num_computed copied to shared memory
 };
+
+// Batches of up to this many requests keep query_start_loc and num_computed
+// in shared memory, so that decoding a tile costs no global load.
+constexpr int kReqCache = 2048;
 
 struct Tile {
   int r, h, u0, ntok;
@@ -140,7 +145,8 @@ struct Layout {
 // cluster tiles run KV head fastest, then groups of C query tiles.
 template <int C>
 __device__ __forceinline__ Tile decode_tile(int ct, int rank, const int32_t* prefix, int R,
-                                            const PrefillParams& p, int tpt) {
+                                            const PrefillParams& p, int tpt,
+                                            const int32_t* qsl, const int32_t* num_computed) {
   int lo = 0, hi = R;  // prefix[lo] <= ct < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -151,9 +157,9 @@ __device__ __forceinline__ Tile decode_tile(int ct, int rank, const int32_t* pre
   const int rem = ct - prefix[lo];
   const int grp = rem / p.hkv;
   t.h = rem - grp * p.hkv;
-  t.qs = __ldg(p.qsl + t.r);
-  const int qlen = __ldg(p.qsl + t.r + 1) - static_cast<int>(t.qs);
-  t.nc = __ldg(p.num_computed + t.r);
+  t.qs = qsl[t.r];
+  const int qlen = qsl[t.r + 1] - static_cast<int>(t.qs);
+  t.nc = num_computed[t.r];
   const int nqt = (qlen + tpt - 1) / tpt;
   const int last = min(grp * C + C, nqt) - 1;  // the cluster's last real query tile
   int qt = grp * C + rank;
@@ -189,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kPrefix);
   int32_t* scan_tmp = prefix + p.num_reqs + 1;
+  int32_t* req_qsl = scan_tmp + 32;            // [R + 1] when cached
+  int32_t* req_nc = req_qsl + p.num_reqs + 1;  // [R]
+  const int32_t* qsl_t = p.cache_reqs ? req_qsl : p.qsl;
+  const int32_t* nc_t = p.cache_reqs ? req_nc : p.num_computed;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = p.num_reqs;
@@ -220,13 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
   }
-  // ---- plan: tiles per prefill request ----
+  // ---- plan: tiles per prefill request (all of a request's metadata in
+  // one round of loads) ----
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    const int qlen = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
+    const int q0 = __ldg(p.qsl + r), q1 = __ldg(p.qsl + r + 1);
+    const int seq = __ldg(p.seq_lens + r), nc = __ldg(p.num_computed + r);
+    if (p.cache_reqs) {
+      req_qsl[r] = q0;
+      req_nc[r] = nc;
+      if (r == R - 1) req_qsl[R] = q1;
+    }
+    const int qlen = q1 - q0;
     int nt = 0;
     if (qlen > 1) {
-      const int seq = __ldg(p.seq_lens + r);
-      if (seq != __ldg(p.num_computed + r) + qlen || (seq + 15) / 16 > p.bt_stride) {
+      if (seq != nc + qlen || (seq + 15) / 16 > p.bt_stride) {
         if (blockIdx.x == 0) atomicOr(p.err, PKV_ERR_METADATA);
       } else {
         nt = ((qlen + tpt - 1) / tpt + C - 1) / C * p.hkv;
@@ -262,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int ct = cid; ct < total && ok; ct += ncl) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
+      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
       const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
       const int nblk = (t.nkeys + 15) / 16;
       // block ids [batch, batch + 32) in `cur`, the next 32 in `nxt`
@@ -352,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_count = 0, k_count = 0, s_count = 0;
       bool ok = true;
       for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
-        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
+        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
         ok = mbar_wait_or_abort(&bars[kQFull], q_count & 1, p.err, abort_flag);
         ++q_count;
         for (int j = 0; j < t.nkt && ok; ++j) {
@@ -392,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t v_count = 0, s_count = 0;
       bool ok = true;
       for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
-        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
+        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
         for (int j = 0; j < t.nkt && ok; ++j) {
           const int vs = v_count % kVStages;
           const int b = s_count % kSBufs;
@@ -453,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int ct = cid; ct < total; ct += ncl) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt);
+      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
       const int u = t.u0 + row / G;  // token of this row within the request
       const bool valid_row = (row / G) < t.ntok;
       const int pos = t.nc + (valid_row ? u : t.u0 + t.ntok - 1);
@@ -611,10 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) grid_dependency_wait();
 }
 
-// Shared memory of one CTA: the layout plus the per-request tile prefix.
+// Shared memory of one CTA: the layout, the per-request tile prefix and, for
+// batches of up to kReqCache requests, query_start_loc and num_computed.
 template <int D>
-static size_t prefill_smem_bytes(int num_reqs) {
-  return 1024 + Layout<D>::kPrefix + 4 * (static_cast<size_t>(num_reqs) + 1) + 4 * 32;
+static size_t prefill_smem_bytes(int num_reqs, bool cache_reqs) {
+  return 1024 + Layout<D>::kPrefix + 4 * (static_cast<size_t>(num_reqs) + 1) + 4 * 32 +
+         (cache_reqs ? 8 * static_cast<size_t>(num_reqs) + 4 : 0);
 }
 
 // Per device: how many clusters of an instantiation fit on the GPU at once.
@@ -628,7 +647,7 @@ template <int D, int C>
 static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap& qmap,
                                     const CUtensorMap& kmap, const CUtensorMap& vmap, int sms,
                                     cudaStream_t stream) {
-  const size_t smem = prefill_smem_bytes<D>(prm.num_reqs);
+  const size_t smem = prefill_smem_bytes<D>(prm.num_reqs, prm.cache_reqs != 0);
   if (smem > kPrefillSmemLimit) return cudaErrorNotSupported;
   auto kern = prefill_tcgen05_kernel<D, C>;
   int dev = 0;
@@ -696,6 +715,7 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, cons
   prm.group = G;
   prm.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   prm.err = a.err;
+  prm.cache_reqs = a.num_reqs <= kReqCache ? 1 : 0;
   // clusters share K/V across query tiles of one request: as many members as
   // the longest request has query tiles, up to 4
   const int tpt = kRows / G;
