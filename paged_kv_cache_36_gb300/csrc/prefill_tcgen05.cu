@@ -221,6 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     prefix[0] = 0;
   }
+  // Cluster members' barriers must exist before any multicast copy or commit
+  // reaches them.  Every thread arrives here, after the initialisation above;
+  // each role waits only just before its first cross-CTA operation, so the
+  // members' launch skew overlaps the plan and the first local copies.
+  if (C > 1) cluster_arrive_release();
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -256,9 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   block_inclusive_scan(prefix + 1, R, scan_tmp);
   __syncthreads();
-  // every member's barriers are initialised before any multicast reaches them
-  if (C > 1) cluster_sync_all();
   const int total = prefix[R];
+  bool cluster_waited = C == 1;  // per warp: the wait half of the barrier above
+  auto cluster_wait_once = [&]() {
+    if (!cluster_waited) {
+      cluster_wait_acquire();
+      cluster_waited = true;
+    }
+  };
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 3) {
@@ -309,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++q_uses;
       }
+      cluster_wait_once();
       for (int j = 0; j < t.nkt && ok; ++j) {
         const int b0 = j * 8;
         if (b0 >= batch + 32) {
@@ -346,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++count;
       }
     }
+    cluster_wait_once();
     // drain: every copy into this CTA's ring (and, in a cluster, every
     // member's release of it) has landed before the CTA may exit
     if (lane == 0) {
@@ -359,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ============================ QK^T issuer ============================
+    cluster_wait_once();
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
       // descriptors are built once; a stage or k-step only adds its byte
@@ -401,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ============================ PV issuer ============================
+    cluster_wait_once();
     if (lane == 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
       // V stage, MN-major: the two 64-dim atoms of a group of 8 keys 1 KiB
@@ -444,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= 4) {
+    cluster_wait_once();
     // ============================ softmax warps ============================
     // Two warps share each 32-lane quadrant of tensor memory (the same 128/4
     // rows): warp half h reads S columns [64 h, 64 h + 64).  They agree on the
@@ -618,6 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  cluster_wait_once();  // warp 3 lanes past its role, and any other warp that skipped it
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
