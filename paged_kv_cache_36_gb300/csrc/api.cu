@@ -272,9 +272,15 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
   ds.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   ds.part_o = reinterpret_cast<float*>(ws + wl.part_o);
   ds.num_slots = wl.slots;
-  cudaError_t e = launch_decode_bf16(a, kblk, vblk, ds, grid, st);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (max_query_len != 1) {
+  // Rows with query length > 1 go to the prefill kernel, launched first (a
+  // normal launch: it reads what reshape_and_cache wrote).  The decode kernel
+  // follows as its programmatic dependent: it reads nothing the prefill
+  // writes, so it is scheduled onto SMs as they free up, and with no decode
+  // rows its launch hides behind the prefill.  A decode-only call launches
+  // the decode kernel normally.
+  const bool prefill = max_query_len != 1;
+  cudaError_t e = cudaSuccess;
+  if (prefill) {
     CUtensorMap qmap, kmap, vmap;
     rc = encode_query_map(&qmap, q, q_stride, num_tokens, num_heads, num_heads / num_kv_heads,
                           head_dim);
@@ -286,6 +292,8 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
     e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
+  e = launch_decode_bf16(a, kblk, vblk, ds, grid, prefill, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
 }
 

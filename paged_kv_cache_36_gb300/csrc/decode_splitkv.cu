@@ -106,9 +106,6 @@ __global__ void __launch_bounds__(288, 1)
   int32_t* prefix = reinterpret_cast<int32_t*>(empty_bar + p.stages);  // [R + 1]
   int32_t* scan_tmp = prefix + R + 1;                                   // [32]
 
-  // the prefill kernel launched after this one reads nothing it writes: let
-  // it be scheduled onto SMs as soon as they free up
-  if (threadIdx.x == 0) grid_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -146,7 +143,13 @@ __global__ void __launch_bounds__(288, 1)
   const int64_t N = prefix[R];
   const int64_t P = N < static_cast<int64_t>(gridDim.x) ? N : static_cast<int64_t>(gridDim.x);
   const int64_t cta = blockIdx.x;
-  if (cta >= P) return;
+  // Launched as a programmatic dependent of the prefill kernel, this grid must
+  // not complete before it: block 0 (here, or in its producer warp below)
+  // waits for the prefill grid before exiting.  It returns at once otherwise.
+  if (cta >= P) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
+    return;
+  }
   const int64_t begin = cta * N / P, end = (cta + 1) * N / P;
 
   // first request of this CTA: prefix[r] <= begin < prefix[r + 1]
@@ -192,7 +195,10 @@ __global__ void __launch_bounds__(288, 1)
               tma_load_4d(kdst + kv_region, &vmap, 0, pb * 16, 0, 0, &full_bar[stage]);
             }
           }
-          if (!__shfl_sync(0xffffffffu, alive, 0)) return;
+          if (!__shfl_sync(0xffffffffu, alive, 0)) {
+            if (blockIdx.x == 0 && lane == 0) grid_dependency_wait();
+            return;
+          }
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
@@ -201,6 +207,7 @@ __global__ void __launch_bounds__(288, 1)
       }
       x = seg_end;
     }
+    if (blockIdx.x == 0 && lane == 0) grid_dependency_wait();
     return;
   }
 
@@ -442,17 +449,28 @@ int decode_grid_size(int device) {
 template <int D, int NT>
 static cudaError_t launch_decode_t(const DecodeParams& prm, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int grid, size_t smem,
-                                   cudaStream_t stream) {
+                                   bool after_prefill, cudaStream_t stream) {
   auto kern = decode_splitkv_kernel<D, NT>;
   const cudaError_t status = raise_smem_limit_once<decode_splitkv_kernel<D, NT>>(kSmemBudget);
   if (status != cudaSuccess) return status;
   if (smem > kSmemBudget) return cudaErrorNotSupported;
-  kern<<<grid, (prm.hkv + 1) * 32, smem, stream>>>(kmap, vmap, prm);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  // after the prefill kernel of the same call: a programmatic dependent of it
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>((prm.hkv + 1) * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prefill ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, prm);
 }
 
 cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               const DecodeScratch& ws, int grid, cudaStream_t stream) {
+                               const DecodeScratch& ws, int grid, bool after_prefill,
+                               cudaStream_t stream) {
   if (a.num_reqs == 0) return cudaSuccess;
   if (a.num_reqs > kDecodeMaxReqs || a.num_kv_heads > 8) return cudaErrorNotSupported;
   DecodeParams prm;
@@ -486,11 +504,11 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const
   const bool wide = prm.group > 8;
   if (prm.group > 16) return cudaErrorNotSupported;
   if (a.head_dim == 128)
-    return wide ? launch_decode_t<128, 2>(prm, kmap, vmap, grid, smem, stream)
-                : launch_decode_t<128, 1>(prm, kmap, vmap, grid, smem, stream);
+    return wide ? launch_decode_t<128, 2>(prm, kmap, vmap, grid, smem, after_prefill, stream)
+                : launch_decode_t<128, 1>(prm, kmap, vmap, grid, smem, after_prefill, stream);
   if (a.head_dim == 64)
-    return wide ? launch_decode_t<64, 2>(prm, kmap, vmap, grid, smem, stream)
-                : launch_decode_t<64, 1>(prm, kmap, vmap, grid, smem, stream);
+    return wide ? launch_decode_t<64, 2>(prm, kmap, vmap, grid, smem, after_prefill, stream)
+                : launch_decode_t<64, 1>(prm, kmap, vmap, grid, smem, after_prefill, stream);
   return cudaErrorNotSupported;
 }
 

@@ -72,7 +72,8 @@ int decode_grid_size(int device);
 
 // Split-KV decode of every request with query length 1 (bf16, mma + TMA).
 cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               const DecodeScratch& ws, int grid, cudaStream_t stream);
+                               const DecodeScratch& ws, int grid, bool after_prefill,
+                               cudaStream_t stream);
 
 // Chunked-prefill attention (bf16, tcgen05 + TMA + TMEM) of every request
 // with query length > 1; qmap is the [T, H, D] query as a (D, H, T) tensor map

@@ -226,6 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // each role waits only just before its first cross-CTA operation, so the
   // members' launch skew overlaps the plan and the first local copies.
   if (C > 1) cluster_arrive_release();
+  // the decode kernel launched after this one reads nothing it writes: let it
+  // be scheduled onto SMs as they free up
+  if (threadIdx.x == 0) grid_launch_dependents();
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -639,9 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (C > 1) cluster_sync_all();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-  // launched as a programmatic dependent of the decode kernel: do not complete
-  // before it, so that work after this kernel sees both
-  if (threadIdx.x == 0) grid_dependency_wait();
 }
 
 // Shared memory of one CTA: the layout, the per-request tile prefix and, for
@@ -694,21 +694,17 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap&
   });
   if (info.status[dev] != cudaSuccess) return info.status[dev];
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // the prefill reads nothing the decode kernel before it writes, so it may be
-  // scheduled while that kernel drains; it waits for it only before exiting
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(info.clusters[dev] * C));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, prm);
 }
 
