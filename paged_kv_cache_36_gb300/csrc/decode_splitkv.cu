@@ -74,6 +74,7 @@ struct DecodeParams {
   float* part_o;
   float* part_ml;
   uint32_t* err;
+  int32_t wait_before_loads;  // wait for the preceding grid before the first cache read
   int32_t stages;
   uint32_t stage_bytes;
 };
@@ -143,9 +144,9 @@ __global__ void __launch_bounds__(288, 1)
   const int64_t N = prefix[R];
   const int64_t P = N < static_cast<int64_t>(gridDim.x) ? N : static_cast<int64_t>(gridDim.x);
   const int64_t cta = blockIdx.x;
-  // Launched as a programmatic dependent of the prefill kernel, this grid must
-  // not complete before it: block 0 (here, or in its producer warp below)
-  // waits for the prefill grid before exiting.  It returns at once otherwise.
+  // Launched as a programmatic dependent, this grid must not complete before
+  // the preceding one: block 0 (here, or in its producer warp below) waits
+  // for it before exiting.  The wait returns at once otherwise.
   if (cta >= P) {
     if (blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
     return;
@@ -165,6 +166,12 @@ __global__ void __launch_bounds__(288, 1)
 
   if (warp == hkv) {
     // ======================= producer warp =======================
+    // Launched as a programmatic dependent, this grid may run its prologue
+    // while the kernel before it finishes.  When that kernel may be
+    // reshape_and_cache, the caches are read only after it has completed; after
+    // the prefill kernel (which reads nothing this grid writes and started
+    // after reshape_and_cache completed) there is nothing to wait for here.
+    if (p.wait_before_loads) grid_dependency_wait();
     int stage = 0;
     uint32_t phase = 0;
     int r = r0;
@@ -456,7 +463,7 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, const CUtensorMap& k
   if (smem > kSmemBudget) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  // after the prefill kernel of the same call: a programmatic dependent of it
+  // a programmatic dependent of the kernel before it in the stream
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -464,7 +471,7 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, const CUtensorMap& k
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = after_prefill ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, prm);
 }
 
@@ -493,6 +500,7 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const
   prm.part_o = ws.part_o;
   prm.part_ml = ws.part_ml;
   prm.err = a.err;
+  prm.wait_before_loads = after_prefill ? 0 : 1;
   prm.stage_bytes = 2u * a.num_kv_heads * (a.head_dim / 64) * 2048u;
   const size_t fixed = 1024 + 16 * kDecodeMaxStages + 4 * (a.num_reqs + 1) + 4 * 32 + 64;
   int stages = static_cast<int>((kSmemBudget - fixed) / prm.stage_bytes);

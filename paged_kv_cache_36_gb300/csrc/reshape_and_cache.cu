@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     int64_t value_stride_v, uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
     const int64_t* __restrict__ slot_mapping, int64_t num_tokens, int64_t num_slots,
     int32_t vec_per_row, uint32_t* __restrict__ err) {
+  // an attention kernel launched as this one's programmatic dependent may
+  // start its prologue now; it waits for this grid before reading the caches
+  if (threadIdx.x == 0) grid_launch_dependents();
   for (int64_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
     const int64_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;
