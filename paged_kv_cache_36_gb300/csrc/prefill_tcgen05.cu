@@ -295,18 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
       const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
       const int nblk = (t.nkeys + 15) / 16;
-      // block ids [batch, batch + 32) in `cur`, the next 32 in `nxt`
-      auto load_ids = [&](int first) -> int32_t {
-        const int b = first + lane;
-        int32_t v = b < nblk ? __ldg(row + b) : 0;
-        if (b < nblk && (v < 0 || v >= p.num_blocks)) {
-          if (is_k) atomicOr(p.err, PKV_ERR_BLOCK_ID);
-          v = p.num_blocks;  // out of the tensor: TMA fills zeros
-        }
-        return v;
-      };
-      int batch = 0;
-      int32_t cur = load_ids(0), nxt = load_ids(32);
       if (is_k) {
         if (lane == 0) {
           if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag)) {
@@ -322,12 +310,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++q_uses;
       }
+      // Block ids [batch, batch + 32) in `cur`, the next 32 in flight in `nxt`.
+      // A batch is checked when it becomes current, by which time its loads
+      // have long completed, so no key tile waits on a block-table read.
+      auto load_ids = [&](int first) -> int32_t {
+        const int b = first + lane;
+        return b < nblk ? __ldg(row + b) : 0;
+      };
+      auto check_ids = [&](int32_t v, int first) -> int32_t {
+        const int b = first + lane;
+        if (b < nblk && (v < 0 || v >= p.num_blocks)) {
+          if (is_k) atomicOr(p.err, PKV_ERR_BLOCK_ID);
+          v = p.num_blocks;  // out of the tensor: TMA fills zeros
+        }
+        return v;
+      };
+      int batch = 0;
+      int32_t cur = load_ids(0), nxt = load_ids(32);
+      cur = check_ids(cur, 0);
       cluster_wait_once();
       for (int j = 0; j < t.nkt && ok; ++j) {
         const int b0 = j * 8;
         if (b0 >= batch + 32) {
           batch += 32;
-          cur = nxt;
+          cur = check_ids(nxt, batch);
           nxt = load_ids(batch + 32);
         }
         const int nvalid = min(8, nblk - b0);
