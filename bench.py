@@ -267,9 +267,10 @@ def build_mixed_step(pkv, device):
     return cfg, step
 
 
-def build_prefill_chunks(pkv, device, copies=CHUNK_COPIES, pool_blocks=4096):
-    """The mixed step's 512-token prefill chunk at [1536, 2048) alone, in its
-    own 4096-block cache: `copies` placements of the request's 128 blocks on
+def build_prefill_chunks(pkv, device, copies=CHUNK_COPIES, pool_blocks=4096, from_start=False):
+    """The mixed step's 512-token prefill chunk at [1536, 2048) alone (or, with
+    from_start, the whole 2048-token prompt as one prefill), in its own
+    4096-block cache: `copies` placements of the request's 128 blocks on
     disjoint random blocks (8.4 MB of K/V each, 168 MB for 20 against a
     129 MB L2), so consecutive calls do not find the previous call's K/V in
     L2."""
@@ -277,6 +278,8 @@ def build_prefill_chunks(pkv, device, copies=CHUNK_COPIES, pool_blocks=4096):
     from workloads.generators import random_block_placement
     cfg = configs.mixed_chunked_step()
     nc, ql = int(cfg.num_computed[0]), int(cfg.query_len[0])
+    if from_start:
+        nc, ql = 0, nc + ql
     n0 = (nc + ql + 15) // 16
     placements = random_block_placement(pool_blocks, [n0] * copies, cfg.name, "chunk copies")
     shape = (pool_blocks, 16, cfg.num_kv_heads, cfg.head_dim)
@@ -294,9 +297,10 @@ def build_prefill_chunks(pkv, device, copies=CHUNK_COPIES, pool_blocks=4096):
         s = torch.from_numpy(b[p // 16] * 16 + p % 16).to(device)
         kf[s] = hist_k
         vf[s] = hist_v
-        chunks.append(DeviceStep(pkv, kc, vc, cfg.q[:ql], cfg.kv.key[o + nc:o + nc + ql],
-                                 cfg.kv.value[o + nc:o + nc + ql], [blk], cfg.query_len[:1],
-                                 cfg.num_computed[:1], cfg.num_heads, device))
+        q = cfg.q[:ql] if ql <= cfg.q.shape[0] else cfg.q[:1].expand(ql, -1, -1).contiguous()
+        chunks.append(DeviceStep(pkv, kc, vc, q, cfg.kv.key[o + nc:o + nc + ql],
+                                 cfg.kv.value[o + nc:o + nc + ql], [blk], np.array([ql]),
+                                 np.array([nc]), cfg.num_heads, device))
     return chunks
 
 
@@ -327,6 +331,171 @@ def graph_time(calls, reps=5):
         times.append(a.elapsed_time(b) / len(calls))
     del g
     return statistics.median(times)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def event_time(fn, n, stream):
+    """Mean device time of fn over n calls, between two events (ms)."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
+    """Supporting measurements beside the headline: the long-context decode
+    (config 4), the continuous-batching trace (config 5) per step,
+    reshape_and_cache at 8192 tokens and the prefill kernel on a 2048-token
+    prompt."""
+    from workloads import configs, trace_spec, generate_arrivals
+    from workloads.generators import random_block_placement
+    res = {}
+    # ---- config 4: 8 decodes over 131072-token histories, 2^20-block pool ----
+    cfg = configs.long_decode_llama70b()
+    H, Hkv, D = cfg.num_heads, cfg.num_kv_heads, cfg.head_dim
+    nb = cfg.num_blocks
+    kc = torch.empty((nb, 16, Hkv, D), dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    used = torch.from_numpy(np.concatenate(cfg.blocks).astype(np.int64)).to(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(127)
+    for c in (kc, vc):
+        for part in used.split(8192):
+            c[part] = torch.randn((part.numel(), 16, Hkv, D), generator=g, device=device,
+                                  dtype=torch.float32).to(torch.bfloat16)
+    R = len(cfg.context)
+    q = torch.randn((R, H, D), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    step = DeviceStep(pkv, kc, vc, q.cpu(), q.cpu()[:, :Hkv], q.cpu()[:, :Hkv], cfg.blocks,
+                      np.ones(R, np.int64), cfg.context - 1, H, device)
+    for _ in range(3):
+        step.attn()
+    ms = event_time(step.attn, 20, stream)
+    res["long_decode"] = {
+        "workload": "Llama-3-70B heads (64/8/128): 8 decodes x 131072-token contexts, "
+                    "2^20-block pool (68.7 GB), random placement",
+        "ms_per_launch": ms, "gbs": step.decode_bytes / (ms * 1e-3) / 1e9,
+        "frac_of_hbm_peak": step.decode_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "algorithmic_bytes_per_launch": step.decode_bytes,
+    }
+    del kc, vc, step, used
+    torch.cuda.empty_cache()
+    # ---- reshape_and_cache at 8192 tokens (inputs rotate over 4 batches) ----
+    T, Hkv, D = 8192, 8, 128
+    nbk = 4 * T // 16 + 64
+    kc = torch.empty((nbk, 16, Hkv, D), dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    blocks = random_block_placement(nbk, [T // 16] * 4, "bench", "k1 8192")
+    batches = []
+    for bi in range(4):
+        b = blocks[bi].astype(np.int64)
+        slots = torch.from_numpy((b[:, None] * 16 + np.arange(16)[None, :]).reshape(-1)).to(device)
+        kn = torch.randn((T, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+        vn = torch.randn((T, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+        batches.append((kn, vn, slots))
+    it = [0]
+    def k1():
+        kn, vn, slots = batches[it[0] % 4]
+        it[0] += 1
+        pkv.reshape_and_cache(kn, vn, kc, vc, slots)
+    for _ in range(8):
+        k1()
+    ms = event_time(k1, 40, stream)
+    k1_bytes = T * (2 * Hkv * D * 2) * 2 + 8 * T
+    res["reshape_and_cache_8192"] = {
+        "workload": "8192 new tokens, 8 KV heads x 128 dims bf16, whole 16-token blocks, "
+                    "4 rotating batches (268 MB of inputs and targets)",
+        "ms_per_launch": ms, "gbs": k1_bytes / (ms * 1e-3) / 1e9,
+        "frac_of_hbm_peak": k1_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "algorithmic_bytes_per_launch": k1_bytes,
+    }
+    del kc, vc, batches
+    torch.cuda.empty_cache()
+    # ---- the prefill kernel on a 2048-token prompt from an empty cache ----
+    prompts = build_prefill_chunks(pkv, device, from_start=True)
+    ms = graph_time([c.attn for c in prompts] * 5)
+    fl = prompts[0].prefill_flops
+    res["prefill_2048"] = {
+        "workload": "one 2048-token prompt from an empty cache, Llama-3-8B heads, "
+                    "20 rotating placements (graph-timed)",
+        "ms_per_call": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+        "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / bf16_peak, "flops": fl,
+    }
+    del prompts
+    torch.cuda.empty_cache()
+    # ---- config 5: the trace, per step (C++ scheduler, device-random K/V/Q) ----
+    spec = trace_spec()
+    H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    sched = pkv.Scheduler(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                          spec.max_model_len, B, spec.num_blocks, spec.max_model_len // B)
+    kc = torch.zeros((spec.num_blocks, B, Hkv, D), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    ws = pkv.new_workspace(spec.max_num_seqs, H, D, device)
+    budget = spec.max_num_batched_tokens
+    qp = torch.randn((budget, H, D), generator=g, device=device).to(torch.bfloat16)
+    kp = torch.randn((budget, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    vp = torch.randn((budget, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    by_step = {}
+    for a in generate_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    per_step = []
+    for st in range(spec.steps):
+        for a in by_step.get(st, []):
+            sched.add_request(a.req_id, a.prompt_len, a.max_output)
+        plan = sched.step()
+        bt, qsl, seq, nc, slots = sched.metadata()
+        T = int(qsl[-1])
+        if T:
+            dev = [torch.from_numpy(x).to(device) for x in (bt, qsl, seq, nc, slots)]
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pkv.reshape_and_cache(kp[:T], vp[:T], kc, vc, dev[4])
+            pkv.paged_attention_varlen(qp[:T], kc, vc, dev[0], dev[1], dev[2], dev[3],
+                                       1.0 / math.sqrt(D), workspace=ws,
+                                       max_query_len=plan["max_query_len"])
+            b.record(stream)
+            b.synchronize()
+            per_step.append((T, a.elapsed_time(b)))
+        sched.finish_step(True)
+    toks = np.array([t for t, _ in per_step], np.float64)
+    mss = np.array([m for _, m in per_step], np.float64)
+    rate = toks / (mss * 1e-3)
+    hist, edges = np.histogram(rate, bins=10)
+    res["trace"] = {
+        "workload": "300-step continuous-batching trace (Poisson arrivals, log-normal prompts, "
+                    "geometric outputs, budget 8192, chunk 512, 16384-block pool), C++ scheduler",
+        "steps_with_tokens": len(per_step), "tokens": int(toks.sum()),
+        "tokens_per_s_per_layer": float(toks.sum() / (mss.sum() * 1e-3)),
+        "per_step_tokens_per_s": {"mean": float(rate.mean()), "p10": float(np.percentile(rate, 10)),
+                                  "median": float(np.median(rate)),
+                                  "p90": float(np.percentile(rate, 90))},
+        "per_step_histogram": {"counts": hist.tolist(), "edges": [float(e) for e in edges]},
+        "preemptions": int(sched.counters()["preemptions"]),
+        "timing": "CUDA events around reshape_and_cache + paged_attention_varlen of each step",
+    }
+    del kc, vc, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_loop(fn_list, steps, stream, per_call=None):
@@ -595,13 +764,17 @@ def main():
         }
         del mstep, chunks
 
+    extra = None
+    if not args.no_secondary:
+        extra = extra_measurements(pkv, device, stream, hbm_peak, bf16_peak)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         torch.set_num_threads(os.cpu_count() or 1)
         o = OracleDecode()
         nbytes, dt, n = o.sample(12.0)
         cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": torch.get_num_threads(),
-               "kind": "oracle",
+               "kind": "oracle", "cpu_model": cpu_model(),
                "sample": f"{n} requests of the headline batch in rotation ({dt:.1f} s): "
                          f"reshape_and_cache scatter of the new token + float64 attention"}
 
@@ -633,6 +806,7 @@ def main():
                             "of the step's inputs -> one H2D copy -> reshape_and_cache -> "
                             "paged_attention_varlen -> D2H out -> stream sync"},
             "secondary": secondary,
+            "extra": extra,
             "cpu_baseline": cpu,
             "gpu_launches": 2 * args.steps,
             "clocks": clk,
