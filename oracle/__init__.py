@@ -10,6 +10,8 @@ It is plain, slow and meant to be read against the pages:
 
 * `paging`    - slot rule, naive cache scatter, per-request block accounting
 * `attention` - dense per-request causal GQA softmax attention in float64
+* `rope`      - table-driven rotary embedding of Q and K (a dense rotation
+                matrix per token) and its fusion with the cache scatter
 * `allocator` - a list-based block allocator with reserve / commit / rollback
 * `scheduler` - a list-based continuous-batching scheduler with recompute
                 preemption, and the step metadata built from its plan
@@ -32,6 +34,9 @@ What pins each part (tests/test_oracle_*.py, run with -m "not gpu"):
   attention       - torch's scaled_dot_product_attention on full prefills,
                     the chunked-equals-full trace on "Chunked Prefill 与
                     Preemption", closed forms, pure-Python brute force
+  rope            - complex multiplication by e^{ia} (numpy), unit-vector
+                    closed forms, orthogonality, the relative-position
+                    property, pass-through of dimensions >= rotary_dim
   allocator       - the conservation law and reserve / commit / rollback
                     protocol of "显存与调度" checked after every transition,
                     telescoping of the incremental block demand
