@@ -366,8 +366,8 @@ def event_time(fn, n, stream):
 def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     """Supporting measurements beside the headline: the long-context decode
     (config 4), the continuous-batching trace (config 5) per step,
-    reshape_and_cache at 8192 tokens and the prefill kernel on a 2048-token
-    prompt."""
+    reshape_and_cache at 8192 tokens with and without the fused RoPE of Q and
+    K, and the prefill kernel on a 2048-token prompt."""
     from workloads import configs, trace_spec, generate_arrivals
     from workloads.generators import random_block_placement
     res = {}
@@ -429,7 +429,35 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         "frac_of_hbm_peak": k1_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
         "algorithmic_bytes_per_launch": k1_bytes,
     }
-    del kc, vc, batches
+    # ---- the same scatter fused with RoPE of Q (32 heads) and K ----
+    from workloads.generators import rope_cos_sin_table
+    H = 32
+    max_pos = 131072
+    table = rope_cos_sin_table(max_pos, D).to(device)
+    starts = [0, 2048, 30000, 120000]  # four 2048-token chunks at different depths
+    pos = torch.from_numpy(np.concatenate([np.arange(a, a + 2048) for a in starts])).to(device)
+    qs = [torch.randn((T, H, D), generator=g, device=device).to(torch.bfloat16) for _ in range(4)]
+    it = [0]
+    def rope_k1():
+        kn, vn, slots = batches[it[0] % 4]
+        pkv.rope_reshape_and_cache(pos, qs[it[0] % 4], kn, vn, kc, vc, slots, table, D)
+        it[0] += 1
+    for _ in range(8):
+        rope_k1()
+    ms = event_time(rope_k1, 40, stream)
+    rope_bytes = T * (2 * H * D * 2 + 2 * (2 * Hkv * D * 2) + D * 4 + 16)
+    res["rope_reshape_and_cache_8192"] = {
+        "workload": "8192 new tokens of Llama-3-8B (32 query heads, 8 KV heads, head_dim 128, "
+                    "bf16, NeoX pairing), positions in four 2048-token chunks, Q rotated in "
+                    "place, rotated K and V scattered to whole 16-token blocks, 4 rotating "
+                    "batches (800 MB of inputs and targets)",
+        "ms_per_launch": ms, "gbs": rope_bytes / (ms * 1e-3) / 1e9,
+        "frac_of_hbm_peak": rope_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "algorithmic_bytes_per_launch": rope_bytes,
+        "bytes_per_token": "Q read + write 16384, K and V read + cache write 8192, "
+                           "table row 512, position + slot 16",
+    }
+    del kc, vc, batches, qs, table
     torch.cuda.empty_cache()
     # ---- the prefill kernel on a 2048-token prompt from an empty cache ----
     prompts = build_prefill_chunks(pkv, device, from_start=True)

@@ -55,6 +55,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_ERR_METADATA 4u     /* seq_len != num_computed + query_len, or a
                                    request longer than its block-table row */
 #define PKV_ERR_TIMEOUT 8u      /* a bounded wait inside a kernel gave up */
+#define PKV_ERR_POSITION 16u    /* a position outside [0, max_position) */
 
 const char* pkv_last_error(void);
 int pkv_version(void);
@@ -83,6 +84,52 @@ int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride
                           const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
                           int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                           int32_t dtype, uint32_t* error_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * rope_reshape_and_cache  [AI Infra, section "Attention Module (以标准GQA +
+ * RoPE为例)": Q and K are rotated by RoPE after the QKV split, the rotation
+ * being a block-diagonal rotation matrix applied element-wise with the row of
+ * a precomputed cos_sin_cache [max_position_embeddings, rotary_dim] picked by
+ * each token's position; then reshape_and_cache scatters K/V by slot_mapping]
+ *
+ * One pass that does both.  For every token t with p = positions[t]:
+ *   row c = cos_sin_cache[p][0 : rotary_dim/2], s = [p][rotary_dim/2 : rotary_dim]
+ *   pair i of a head is (a, b) = (2i, 2i+1) if is_neox == 0, else
+ *   (i, i + rotary_dim/2); (x_a, x_b) -> (x_a c_i - x_b s_i, x_b c_i + x_a s_i);
+ *   dimensions >= rotary_dim are unchanged.
+ *   query[t][h]  <- rotated, in place, for every query head h;
+ *   key_cache[slot] <- rotated key[t];  value_cache[slot] <- value[t]
+ *     (slot = slot_mapping[t]; slot < 0 skips the scatter, slot >=
+ *     num_blocks * block_size skips it and sets PKV_ERR_SLOT);
+ *   key_out[t] <- rotated key[t] if key_out is not NULL (it may equal key).
+ * A position outside [0, max_position) sets PKV_ERR_POSITION and the token is
+ * left untouched (query not rotated, nothing scattered).  Arithmetic is fp32;
+ * bf16 results are rounded to nearest even.
+ *
+ * positions, slot_mapping: device int64 [num_tokens].
+ * query: device [num_tokens, num_heads, head_dim], token stride query_stride.
+ * key, value (and key_out): device [num_tokens, num_kv_heads, head_dim], token
+ *   strides key_stride / value_stride (key_out uses key_stride).
+ * key_cache, value_cache: device [num_blocks, block_size, num_kv_heads,
+ *   head_dim].  cos_sin_cache: device float32 [max_position, rotary_dim].
+ * dtype (of query, key, value, caches): PKV_BF16 or PKV_F32.  Strides in
+ *   elements.  All base pointers and token strides 16-byte aligned; head_dim
+ *   * element size a multiple of 16 bytes; 0 < rotary_dim <= head_dim with
+ *   rotary_dim / 2 (NeoX) or rotary_dim (interleaved) times the element size
+ *   a multiple of 16 bytes; otherwise PKV_E_INVALID / PKV_E_UNSUPPORTED and
+ *   nothing is launched.
+ * The attention entry points may follow this call directly on the stream:
+ *   they read query and the caches only after it has completed.
+ * ---------------------------------------------------------------------- */
+int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t query_stride,
+                               int32_t num_heads, const void* key, int64_t key_stride,
+                               void* key_out, const void* value, int64_t value_stride,
+                               void* key_cache, void* value_cache, const int64_t* slot_mapping,
+                               const float* cos_sin_cache, int64_t max_position,
+                               int32_t rotary_dim, int32_t is_neox, int64_t num_tokens,
+                               int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t dtype, uint32_t* error_word,
+                               void* stream);
 
 /* ------------------------------------------------------------------------
  * paged_attention_varlen  [AI Infra, section "Attention Module (以标准GQA +
@@ -130,6 +177,52 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
                                int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                int32_t dtype, int32_t max_query_len, void* workspace,
                                size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * rope_reshape_and_cache  [AI Infra, section "Attention Module (以标准GQA +
+ * RoPE为例)": Q and K are rotated by RoPE after the QKV split, the rotation
+ * being a block-diagonal rotation matrix applied element-wise with the row of
+ * a precomputed cos_sin_cache [max_position_embeddings, rotary_dim] picked by
+ * each token's position; then reshape_and_cache scatters K/V by slot_mapping]
+ *
+ * One pass that does both.  For every token t with p = positions[t]:
+ *   row c = cos_sin_cache[p][0 : rotary_dim/2], s = [p][rotary_dim/2 : rotary_dim]
+ *   pair i of a head is (a, b) = (2i, 2i+1) if is_neox == 0, else
+ *   (i, i + rotary_dim/2); (x_a, x_b) -> (x_a c_i - x_b s_i, x_b c_i + x_a s_i);
+ *   dimensions >= rotary_dim are unchanged.
+ *   query[t][h]  <- rotated, in place, for every query head h;
+ *   key_cache[slot] <- rotated key[t];  value_cache[slot] <- value[t]
+ *     (slot = slot_mapping[t]; slot < 0 skips the scatter, slot >=
+ *     num_blocks * block_size skips it and sets PKV_ERR_SLOT);
+ *   key_out[t] <- rotated key[t] if key_out is not NULL (it may equal key).
+ * A position outside [0, max_position) sets PKV_ERR_POSITION and the token is
+ * left untouched (query not rotated, nothing scattered).  Arithmetic is fp32;
+ * bf16 results are rounded to nearest even.
+ *
+ * positions, slot_mapping: device int64 [num_tokens].
+ * query: device [num_tokens, num_heads, head_dim], token stride query_stride.
+ * key, value (and key_out): device [num_tokens, num_kv_heads, head_dim], token
+ *   strides key_stride / value_stride (key_out uses key_stride).
+ * key_cache, value_cache: device [num_blocks, block_size, num_kv_heads,
+ *   head_dim].  cos_sin_cache: device float32 [max_position, rotary_dim].
+ * dtype (of query, key, value, caches): PKV_BF16 or PKV_F32.  Strides in
+ *   elements.  All base pointers and token strides 16-byte aligned; head_dim
+ *   * element size a multiple of 16 bytes; 0 < rotary_dim <= head_dim with
+ *   rotary_dim / 2 (NeoX) or rotary_dim (interleaved) times the element size
+ *   a multiple of 16 bytes; otherwise PKV_E_INVALID / PKV_E_UNSUPPORTED and
+ *   nothing is launched.
+ * The attention entry points may follow this call directly on the stream:
+ *   they read query and the caches only after it has completed.
+ * ---------------------------------------------------------------------- */
+int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t query_stride,
+                               int32_t num_heads, const void* key, int64_t key_stride,
+                               void* key_out, const void* value, int64_t value_stride,
+                               void* key_cache, void* value_cache, const int64_t* slot_mapping,
+                               const float* cos_sin_cache, int64_t max_position,
+                               int32_t rotary_dim, int32_t is_neox, int64_t num_tokens,
+                               int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t dtype, uint32_t* error_word,
+                               void* stream);
 
 /* ------------------------------------------------------------------------
  * paged_attention_varlen without a workspace.  The pages have no counterpart:

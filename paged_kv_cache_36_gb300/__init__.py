@@ -14,11 +14,11 @@ import ctypes as C
 import numpy as np
 
 from . import _ffi
-from ._ffi import (ERR_BLOCK_ID, ERR_METADATA, ERR_SLOT, ERR_TIMEOUT, PKV_BF16,  # noqa: F401
-                   PKV_F32)
+from ._ffi import (ERR_BLOCK_ID, ERR_METADATA, ERR_POSITION, ERR_SLOT, ERR_TIMEOUT,  # noqa: F401
+                   PKV_BF16, PKV_F32)
 
 __all__ = [
-    "PkvError", "lib", "reshape_and_cache", "attention_workspace_bytes", "new_workspace",
+    "PkvError", "lib", "reshape_and_cache", "rope_reshape_and_cache", "attention_workspace_bytes", "new_workspace",
     "paged_attention_varlen", "read_error_word", "build_slot_mapping", "Allocator", "Scheduler",
 ]
 
@@ -82,6 +82,38 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, error_wo
         int(slot_mapping.shape[0]), nb, bs, hkv, d, _dtype_code(key_cache),
         error_word.data_ptr() if error_word is not None else None, _stream_ptr(stream))
     _check(code, "reshape_and_cache")
+
+
+def rope_reshape_and_cache(positions, query, key, value, key_cache, value_cache, slot_mapping,
+                           cos_sin_cache, rotary_dim: int | None = None, is_neox: bool = True,
+                           key_out=None, error_word=None, stream=None) -> None:
+    """Rotate query [T, H, D] in place and key [T, Hkv, D] by cos_sin_cache[positions]
+    (float32 [max_position, rotary_dim]), and scatter the rotated key and value
+    into the caches [NB, B, Hkv, D] at slot_mapping (int64 [T]).  key_out, if
+    given, receives the rotated key too (it may be `key`)."""
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()
+            and cos_sin_cache.is_contiguous()):
+        raise ValueError("caches and cos_sin_cache must be contiguous")
+    import torch
+    if cos_sin_cache.dtype != torch.float32 or cos_sin_cache.dim() != 2:
+        raise TypeError("cos_sin_cache must be float32 [max_position, rotary_dim]")
+    if positions.dtype != torch.int64 or slot_mapping.dtype != torch.int64:
+        raise TypeError("positions and slot_mapping must be int64")
+    nb, bs, hkv, d = key_cache.shape
+    rd = int(cos_sin_cache.shape[1]) if rotary_dim is None else int(rotary_dim)
+    if rd != cos_sin_cache.shape[1]:
+        raise ValueError("rotary_dim must equal cos_sin_cache.shape[1]")
+    ks = _token_stride(key)
+    if key_out is not None and _token_stride(key_out) != ks:
+        raise ValueError("key_out must have key's token stride")
+    code = lib().pkv_rope_reshape_and_cache(
+        positions.data_ptr(), query.data_ptr(), _token_stride(query), int(query.shape[1]),
+        key.data_ptr(), ks, key_out.data_ptr() if key_out is not None else None,
+        value.data_ptr(), _token_stride(value), key_cache.data_ptr(), value_cache.data_ptr(),
+        slot_mapping.data_ptr(), cos_sin_cache.data_ptr(), int(cos_sin_cache.shape[0]), rd,
+        int(bool(is_neox)), int(positions.shape[0]), nb, bs, hkv, d, _dtype_code(key_cache),
+        error_word.data_ptr() if error_word is not None else None, _stream_ptr(stream))
+    _check(code, "rope_reshape_and_cache")
 
 
 def attention_workspace_bytes(num_reqs: int, num_heads: int, head_dim: int) -> int:

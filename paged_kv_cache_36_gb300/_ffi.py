@@ -17,7 +17,7 @@ ERRORS = {
     -5: "PKV_E_STATE", -6: "PKV_E_UNKNOWN_REQ", -7: "PKV_E_CUDA", -8: "PKV_E_CAPACITY",
 }
 PKV_F32, PKV_BF16 = 0, 1
-ERR_BLOCK_ID, ERR_SLOT, ERR_METADATA, ERR_TIMEOUT = 1, 2, 4, 8
+ERR_BLOCK_ID, ERR_SLOT, ERR_METADATA, ERR_TIMEOUT, ERR_POSITION = 1, 2, 4, 8, 16
 
 i32, i64, u32, u64, f32, f64 = C.c_int32, C.c_int64, C.c_uint32, C.c_uint64, C.c_float, C.c_double
 vp, sz = C.c_void_p, C.c_size_t
@@ -52,6 +52,9 @@ SIGNATURES = {
     "pkv_version": (C.c_int, []),
     "pkv_reshape_and_cache": (C.c_int, [vp, vp, i64, i64, vp, vp, vp, i64, i64, i32, i32, i32,
                                         i32, vp, vp]),
+    "pkv_rope_reshape_and_cache": (C.c_int, [vp, vp, i64, i32, vp, i64, vp, vp, i64, vp, vp,
+                                             vp, vp, i64, i32, i32, i64, i64, i32, i32, i32,
+                                             i32, vp, vp]),
     "pkv_attention_workspace_bytes": (sz, [i32, i32, i32]),
     "pkv_paged_attention_varlen": (C.c_int, [vp, i64, vp, vp, vp, i32, vp, vp, vp, f32, vp, i64,
                                              i64, i32, i64, i32, i32, i32, i32, i32, i32, vp, sz,

@@ -189,6 +189,68 @@ int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "reshape_and_cache launch");
 }
 
+int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t query_stride,
+                               int32_t num_heads, const void* key, int64_t key_stride,
+                               void* key_out, const void* value, int64_t value_stride,
+                               void* key_cache, void* value_cache, const int64_t* slot_mapping,
+                               const float* cos_sin_cache, int64_t max_position,
+                               int32_t rotary_dim, int32_t is_neox, int64_t num_tokens,
+                               int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t dtype, uint32_t* error_word,
+                               void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_heads <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0 || max_position <= 0)
+    return fail(PKV_E_INVALID, "pkv_rope_reshape_and_cache: sizes must be positive");
+  if (dtype != PKV_F32 && dtype != PKV_BF16)
+    return fail(PKV_E_UNSUPPORTED, "pkv_rope_reshape_and_cache: dtype %d", dtype);
+  if (rotary_dim <= 0 || rotary_dim > head_dim || rotary_dim % 2)
+    return fail(PKV_E_INVALID, "pkv_rope_reshape_and_cache: rotary_dim %d (head_dim %d)",
+                rotary_dim, head_dim);
+  const int64_t esize = dtype == PKV_F32 ? 4 : 2;
+  const int64_t item = (is_neox ? rotary_dim / 2 : rotary_dim) * esize;
+  if ((head_dim * esize) % 16 || item % 16)
+    return fail(PKV_E_UNSUPPORTED,
+                "pkv_rope_reshape_and_cache: head_dim and the rotated %s must be multiples of "
+                "16 bytes", is_neox ? "half" : "part");
+  if (num_tokens == 0) return PKV_OK;
+  if (!positions || !query || !key || !value || !key_cache || !value_cache || !slot_mapping ||
+      !cos_sin_cache)
+    return fail(PKV_E_INVALID, "pkv_rope_reshape_and_cache: null pointer");
+  if ((query_stride * esize) % 16 || (key_stride * esize) % 16 || (value_stride * esize) % 16 ||
+      !aligned16(query) || !aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
+      !aligned16(value_cache) || !aligned16(cos_sin_cache) || (key_out && !aligned16(key_out)))
+    return fail(PKV_E_INVALID, "pkv_rope_reshape_and_cache: strides and bases must be 16-byte aligned");
+  const int64_t kv_row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (query_stride < static_cast<int64_t>(num_heads) * head_dim || key_stride < kv_row ||
+      value_stride < kv_row)
+    return fail(PKV_E_INVALID, "pkv_rope_reshape_and_cache: token stride shorter than a row");
+  RopeArgs a;
+  a.positions = positions;
+  a.query = query;
+  a.query_stride = query_stride;
+  a.key = key;
+  a.key_stride = key_stride;
+  a.key_out = key_out;
+  a.value = value;
+  a.value_stride = value_stride;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.slot_mapping = slot_mapping;
+  a.cos_sin_cache = cos_sin_cache;
+  a.max_position = max_position;
+  a.num_tokens = num_tokens;
+  a.num_slots = num_blocks * block_size;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.rotary_dim = rotary_dim;
+  a.is_neox = is_neox != 0;
+  a.bf16 = dtype == PKV_BF16;
+  a.err = error_word;
+  cudaError_t e = launch_rope_reshape_and_cache(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "rope_reshape_and_cache launch");
+}
+
 size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_t head_dim) {
   if (num_reqs < 0 || num_heads <= 0 || head_dim <= 0) return 0;
   return workspace_layout(num_reqs, num_heads, head_dim, current_grid()).total;

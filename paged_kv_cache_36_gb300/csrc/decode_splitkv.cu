@@ -74,7 +74,7 @@ struct DecodeParams {
   float* part_o;
   float* part_ml;
   uint32_t* err;
-  int32_t wait_before_loads;  // wait for the preceding grid before the first cache read
+  int32_t wait_before_loads;  // wait for the preceding grid before reading Q or the caches
   int32_t stages;
   uint32_t stage_bytes;
 };
@@ -167,10 +167,11 @@ __global__ void __launch_bounds__(288, 1)
   if (warp == hkv) {
     // ======================= producer warp =======================
     // Launched as a programmatic dependent, this grid may run its prologue
-    // while the kernel before it finishes.  When that kernel may be
-    // reshape_and_cache, the caches are read only after it has completed; after
-    // the prefill kernel (which reads nothing this grid writes and started
-    // after reshape_and_cache completed) there is nothing to wait for here.
+    // while the kernel before it finishes.  When that kernel may be the cache
+    // write (with or without RoPE, which also rewrites Q), the caches and Q
+    // are read only after it has completed; after the prefill kernel (which
+    // writes nothing this grid reads and started after the cache write
+    // completed) there is nothing to wait for here.
     if (p.wait_before_loads) grid_dependency_wait();
     int stage = 0;
     uint32_t phase = 0;
@@ -219,6 +220,9 @@ __global__ void __launch_bounds__(288, 1)
   }
 
   // ======================= consumer warps (one per KV head) =======================
+  // Q may still be being rotated in place by the preceding kernel (see the
+  // producer's wait above)
+  if (p.wait_before_loads) grid_dependency_wait();
   const int h = warp;
   const int G = p.group;
   const int gid = lane >> 2, tid = lane & 3;

@@ -67,6 +67,34 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                                      int64_t num_slots, int64_t row_bytes, uint32_t* err,
                                      cudaStream_t stream);
 
+// Fused RoPE + reshape_and_cache (sizes and strides in elements).
+struct RopeArgs {
+  const int64_t* positions;
+  void* query;
+  int64_t query_stride;
+  const void* key;
+  int64_t key_stride;
+  void* key_out;              // may be null
+  const void* value;
+  int64_t value_stride;
+  void* key_cache;
+  void* value_cache;
+  const int64_t* slot_mapping;
+  const float* cos_sin_cache;
+  int64_t max_position;
+  int64_t num_tokens;
+  int64_t num_slots;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t rotary_dim;
+  bool is_neox;
+  bool bf16;
+  uint32_t* err;
+};
+
+cudaError_t launch_rope_reshape_and_cache(const RopeArgs& a, cudaStream_t stream);
+
 // Grid size (CTAs) of the persistent split-KV decode kernel on this device.
 int decode_grid_size(int device);
 

@@ -63,3 +63,26 @@ def test_bad_arguments_rejected_without_gpu(libpkv):
     assert rc == -2
     rc = L.pkv_reshape_and_cache(None, None, 0, 0, None, None, None, 1, 16, 16, 2, 64, 7, None, None)
     assert rc == -2
+
+
+def test_rope_argument_checks(libpkv):
+    """Host-side validation of the fused RoPE entry point (nothing launches)."""
+    import paged_kv_cache_36_gb300 as pkv
+    from paged_kv_cache_36_gb300 import _ffi
+    lib = pkv.lib()
+    f = lib.pkv_rope_reshape_and_cache
+
+    def call(rd=128, neox=1, T=0, D=128, dtype=_ffi.PKV_BF16, max_pos=16):
+        return f(None, None, 32 * D, 32, None, 8 * D, None, None, 8 * D, None, None, None, None,
+                 max_pos, rd, neox, T, 64, 16, 8, D, dtype, None, None)
+
+    assert call() == 0                                   # zero tokens: nothing to do
+    assert call(rd=127) == -1                            # odd rotary_dim
+    assert call(rd=256) == -1                            # rotary_dim > head_dim
+    assert call(rd=0) == -1
+    assert call(max_pos=0) == -1
+    assert call(dtype=5) == -2                           # unknown dtype
+    assert call(rd=8, neox=1) == -2                      # NeoX half of 4 bf16 = 8 bytes
+    assert call(rd=8, neox=0) == 0                       # interleaved 8 bf16 = 16 bytes
+    assert call(T=3) == -1                               # null pointers with tokens to do
+    assert b"null pointer" in lib.pkv_last_error()

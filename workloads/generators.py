@@ -89,6 +89,20 @@ def random_block_placement(pool_blocks: int, counts, *name) -> list[np.ndarray]:
     return out
 
 
+def rope_cos_sin_table(max_position: int, rotary_dim: int, base: float = 500000.0) -> torch.Tensor:
+    """A synthetic cos_sin_cache: float32 [max_position, rotary_dim], row p =
+    [cos(p w_0) .. cos(p w_{n-1}), sin(p w_0) .. sin(p w_{n-1})] with
+    n = rotary_dim / 2 and w_i = base^(-2i / rotary_dim) (the RoFormer angle
+    schedule; base 500000 is Llama-3's).  Evaluated in float64, rounded once
+    to float32.  Only the table's shape and row layout come from the pages;
+    the angles are a plausible input, not part of the method.
+    """
+    half = rotary_dim // 2
+    w = base ** (-2.0 * np.arange(half, dtype=np.float64) / rotary_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * w[None, :]
+    return torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+
+
 # ---------------------------------------------------------------------------
 # counter-hashed row pools
 # ---------------------------------------------------------------------------
