@@ -127,18 +127,43 @@ def _run_and_check(T, H, Hkv, D, rd, dtype, is_neox, NB=64, name="rope", key_out
         assert torch.equal(_bits(dk.cpu()), _bits(k)), "key must be left unchanged"
 
 
+@pytest.mark.parametrize("T", [300, 1500])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("is_neox", [True, False])
 @pytest.mark.parametrize("H,Hkv,D,rd", [(32, 8, 128, 128), (8, 2, 128, 64), (4, 1, 64, 64),
-                                        (6, 2, 64, 32)])
-def test_rope_reshape_and_cache_parity(dtype, is_neox, H, Hkv, D, rd):
-    # 300 tokens: 37 full 8-warp blocks and a ragged tail; every 17th a padding token
-    _run_and_check(300, H, Hkv, D, rd, dtype, is_neox, name=f"rope{H}_{D}_{rd}")
+                                        (6, 2, 64, 32), (8, 2, 128, 48)])
+def test_rope_reshape_and_cache_parity(T, dtype, is_neox, H, Hkv, D, rd):
+    # 300 tokens take the staged form (one to a few tokens per CTA, a ragged
+    # split), 1500 the one-warp-per-token form (a ragged last block of 8
+    # warps); rotary_dim 48 (3 or 6 items per head) always takes the warp
+    # form.  Every 17th token is a padding token.
+    _run_and_check(T, H, Hkv, D, rd, dtype, is_neox, NB=(T + 15) // 16 + 48,
+                   name=f"rope{T}_{H}_{D}_{rd}")
+
+
+@pytest.mark.parametrize("is_neox", [True, False])
+def test_rope_rows_too_large_for_the_ring(is_neox):
+    """128 query heads of 256 dims (64 KiB of Q per token in bf16): three
+    ring stages do not fit in shared memory, the warp form takes over."""
+    _run_and_check(45, 128, 8, 256, 256, torch.bfloat16, is_neox, NB=8, name="ropebig")
+
+
+def test_rope_many_tokens_per_cta():
+    """160000 tokens of 8 + 2 heads: each CTA of the staged form takes about
+    70 consecutive tokens, so it reloads its positions past the first 32 and
+    wraps its 4-stage ring many times.  V rows and untouched slots are checked
+    bit for bit, Q and K of 2048 sampled tokens against the oracle."""
+    T, H, Hkv, D, NB, B = 160000, 8, 2, 128, 10240, 16
+    _large_case_check("ropemany", T, H, Hkv, D, NB, B,
+                      uniform_int(0, 4095, T, "ropemany", "pos"), 4096,
+                      random_block_placement(NB * B, [T], "ropemany", "slots")[0].astype(np.int64))
 
 
 @pytest.mark.parametrize("mode", ["inplace", "separate"])
 def test_rope_key_out(mode):
     _run_and_check(77, 16, 4, 128, 128, torch.bfloat16, True, name="rope_keyout", key_out_mode=mode)
+    _run_and_check(1100, 16, 4, 128, 128, torch.bfloat16, True, NB=120, name="rope_keyout_w",
+                   key_out_mode=mode)
 
 
 def test_rope_one_token_and_empty():
@@ -156,12 +181,13 @@ def test_rope_one_token_and_empty():
     assert bool((kc == 1).all()) and bool((vc == 1).all())
 
 
-def test_rope_bad_position_and_slot():
+@pytest.mark.parametrize("T,NB", [(40, 8), (1200, 80)])
+def test_rope_bad_position_and_slot(T, NB):
     """A position outside the table leaves its token untouched and flags
     PKV_ERR_POSITION; a slot past the pool is skipped and flags PKV_ERR_SLOT
-    (the token's Q is still rotated)."""
+    (the token's Q is still rotated).  Both forms (40 and 1200 tokens)."""
     pkv = _pkv()
-    T, H, Hkv, D, NB, B, max_pos = 40, 8, 2, 128, 8, 16, 64
+    H, Hkv, D, B, max_pos = 8, 2, 128, 16, 64
     q = randn_fp32((T, H, D), "ropebad", "q", dtype=torch.bfloat16)
     k = randn_fp32((T, Hkv, D), "ropebad", "k", dtype=torch.bfloat16)
     v = randn_fp32((T, Hkv, D), "ropebad", "v", dtype=torch.bfloat16)
@@ -203,23 +229,11 @@ def test_rope_bad_position_and_slot():
     assert torch.equal(_bits(dvc.cpu()), _bits(torch.from_numpy(vc64).to(torch.bfloat16)))
 
 
-def test_rope_full_size_llama8b_prefill_chunk():
-    """8192 tokens of Llama-3-8B (32 query heads, 8 KV heads, head_dim 128,
-    NeoX pairing, bf16) scattered over a 4096-block pool: every V row and
-    every untouched slot checked bit for bit, Q and K of 1024 sampled tokens
-    against the oracle."""
+def _large_case_check(name, T, H, Hkv, D, NB, B, pos, max_pos, slots, sample_n=2048):
     pkv = _pkv()
-    T, H, Hkv, D, NB, B, max_pos = 8192, 32, 8, 128, 4096, 16, 131072
-    name = "rope8192"
     q = randn_fp32((T, H, D), name, "q", dtype=torch.bfloat16)
     k = randn_fp32((T, Hkv, D), name, "k", dtype=torch.bfloat16)
     v = randn_fp32((T, Hkv, D), name, "v", dtype=torch.bfloat16)
-    # four requests, 2048 new tokens each, at different depths of their context
-    starts = [0, 2048, 30000, 120000]
-    pos = np.concatenate([np.arange(s, s + 2048) for s in starts]).astype(np.int64)
-    blocks = random_block_placement(NB, [128] * 4, name, "placement")
-    slots = np.concatenate([b.astype(np.int64)[np.arange(2048) // B] * B + np.arange(2048) % B
-                            for b in blocks])
     table = rope_cos_sin_table(max_pos, D)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     dkc = torch.zeros(NB, B, Hkv, D, dtype=torch.bfloat16, device="cuda")
@@ -235,13 +249,29 @@ def test_rope_full_size_llama8b_prefill_chunk():
     mask = torch.ones(NB * B, dtype=torch.bool, device="cuda")
     mask[dslots] = False
     assert not bool(_bits(kflat[mask]).any()) and not bool(_bits(vflat[mask]).any())
-    sample = np.sort(np.random.default_rng(5).choice(T, 1024, replace=False))
+    assert torch.equal(_bits(dk), _bits(k.cuda())), "key must be left unchanged"
+    sample = np.sort(np.random.default_rng(5).choice(T, sample_n, replace=False))
     q_rot = rope.apply_rope(q[sample], pos[sample], table, D, True)
     k_rot = rope.apply_rope(k[sample], pos[sample], table, D, True)
     _assert_rotated(dq.cpu()[sample], q_rot, _magnitude(q[sample], pos[sample], table, D, True),
                     torch.bfloat16, "query")
     _assert_rotated(kflat[dslots[torch.from_numpy(sample).cuda()]], k_rot,
                     _magnitude(k[sample], pos[sample], table, D, True), torch.bfloat16, "key")
+
+
+def test_rope_full_size_llama8b_prefill_chunk():
+    """8192 tokens of Llama-3-8B (32 query heads, 8 KV heads, head_dim 128,
+    NeoX pairing, bf16) scattered over a 4096-block pool, positions in four
+    2048-token chunks at depths up to 122047: every V row and every untouched
+    slot checked bit for bit, Q and K of 1024 sampled tokens against the
+    oracle."""
+    T, NB, B = 8192, 4096, 16
+    starts = [0, 2048, 30000, 120000]
+    pos = np.concatenate([np.arange(s, s + 2048) for s in starts]).astype(np.int64)
+    blocks = random_block_placement(NB, [128] * 4, "rope8192", "placement")
+    slots = np.concatenate([b.astype(np.int64)[np.arange(2048) // B] * B + np.arange(2048) % B
+                            for b in blocks])
+    _large_case_check("rope8192", T, 32, 8, 128, NB, B, pos, 131072, slots, sample_n=1024)
 
 
 # ---------------------------------------------------------------- followed by attention
