@@ -286,7 +286,8 @@ int pkv_build_slot_mapping(const int32_t* block_table, int32_t block_table_strid
  * each request's table and adds s_i to T_i; rollback() returns the reserved
  * blocks to the front of the free list so it is exactly as before.
  * free_request() releases a request's committed blocks (block-table order),
- * then any of its reserved ones, to the back of the free list.
+ * then any of its reserved ones, to the back of the free list (with prefix
+ * sharing, only blocks no other request holds; indexed ones become cached).
  * ---------------------------------------------------------------------- */
 typedef struct pkv_alloc pkv_alloc;
 
@@ -294,7 +295,7 @@ typedef struct {
   int64_t capacity;        /* q_capacity */
   int64_t free;            /* q_free */
   int64_t reserved;        /* q_reserved (open plan) */
-  int64_t committed;       /* q_committed */
+  int64_t committed;       /* q_committed = q_live, the union of the block sets */
   int64_t num_requests;    /* requests holding committed blocks */
   int64_t tail_waste;      /* sum of w_i over committed requests, in token slots */
   int64_t alloc_failures;  /* reserve() calls refused for lack of blocks */
@@ -316,9 +317,74 @@ int pkv_alloc_table(const pkv_alloc* a, int32_t req_id, int32_t* out, int32_t ca
 int64_t pkv_alloc_held_tokens(const pkv_alloc* a, int32_t req_id);
 /* the free list, front first; returns its length or an error */
 int pkv_alloc_free_list(const pkv_alloc* a, int32_t* out, int32_t capacity);
-/* verifies conservation, q_i = ceil(T_i / B), and that every block id is in
- * exactly one place; PKV_OK or PKV_E_STATE */
+/* verifies conservation, q_i = ceil(T_i / B), that every block id is in
+ * exactly one place, holder counts, and the prefix index's tree; PKV_OK or
+ * PKV_E_STATE */
 int pkv_alloc_check(const pkv_alloc* a);
+
+/* ------------------------------------------------------------------------
+ * Prefix sharing  [显存调度, section "共享前缀会改变块的所有权": identical KV
+ * prefixes share physical blocks; q_live = |union of the requests' block
+ * sets| <= q_capacity; r_p counts the active requests and the retaining cache
+ * owner of block p, which is recycled only at r_p = 0; a prefix index finds
+ * the longest reusable prefix and evicts reusable leaf entries under memory
+ * pressure; full shared blocks are immutable, a shared block still being
+ * written is copied first (copy-on-write).  Section "同时验证分配器与调度器":
+ * shared blocks are recycled only after the last reference; an incompatible
+ * namespace never hits.]
+ *
+ * The cache identity of a block is (namespace, the block it extends, its
+ * block_size token ids): the namespace stands for model version, adapter,
+ * position handling, cache format, modality and tenant.  Only full blocks
+ * wholly inside a prompt registered with match_prefix are indexed, at the
+ * commit that completes them.  A block held by no request but retained by the
+ * index is "cached": q_free + q_reserved + q_live + q_cached = q_capacity,
+ * where pkv_alloc_stats.committed is q_live.  reserve() evicts the oldest
+ * cached blocks that no indexed block extends (to the back of the free list)
+ * when a plan fits in q_free + q_cached but not in q_free; evictions stand
+ * after a rollback.  A plan entry that writes into a partial last block held
+ * by another request too gets one extra block: its table shows the copy, and
+ * pkv_alloc_pending_copies lists (source, destination) for the device copy
+ * (pkv_copy_blocks) that must run before the step writes; in plan order, the
+ * last writer of such a block keeps the original.  free_request() returns
+ * how many of the request's blocks no request holds any more.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int64_t lookups;         /* match_prefix calls */
+  int64_t hits;            /* calls that matched at least one block */
+  int64_t matched_tokens;  /* prefix tokens served from the index */
+  int64_t evictions;       /* blocks evicted from the index */
+  int64_t cow_copies;      /* copy-on-write copies committed */
+  int64_t indexed;         /* blocks in the index */
+  int64_t shared;          /* live blocks held by two or more requests */
+  int64_t cached;          /* q_cached */
+} pkv_prefix_stats;
+
+/* Registers req_id's prompt (tokens[0..n)) for indexing and gives it the
+ * longest indexed prefix of at most n - 1 tokens in namespace ns: its table
+ * starts with those blocks and T_i = the matched token count, which is
+ * returned.  req_id must hold nothing and no reservation may be open
+ * (PKV_E_STATE). */
+int pkv_alloc_match_prefix(pkv_alloc* a, int32_t req_id, uint64_t ns, const int32_t* tokens,
+                           int32_t n);
+/* The matched token count match_prefix would return, with no side effects;
+ * *cached_blocks (if not NULL) receives how many of those blocks are cached
+ * now (they leave q_cached when matched). */
+int pkv_alloc_peek_prefix(const pkv_alloc* a, uint64_t ns, const int32_t* tokens, int32_t n,
+                          int32_t* cached_blocks);
+/* child_id starts with parent_id's committed blocks and token count (no
+ * prompt registration); e.g. parallel samples of one prompt. */
+int pkv_alloc_fork(pkv_alloc* a, int32_t parent_id, int32_t child_id);
+/* (source, destination) block pairs of the open plan's copy-on-writes into
+ * pairs[2 * capacity]; returns the count. */
+int pkv_alloc_pending_copies(const pkv_alloc* a, int32_t* pairs, int32_t capacity);
+int pkv_alloc_get_prefix_stats(const pkv_alloc* a, pkv_prefix_stats* out);
+/* r_p of a block: requests holding it plus one if the index retains it */
+int pkv_alloc_ref_count(const pkv_alloc* a, int32_t block);
+/* the cached blocks, oldest release first; returns the count */
+int pkv_alloc_cached_list(const pkv_alloc* a, int32_t* out, int32_t capacity);
+/* q_free + q_cached: the blocks a plan may take */
+int64_t pkv_alloc_available(const pkv_alloc* a);
 
 /* ------------------------------------------------------------------------
  * Continuous-batching scheduler (host)  [AI Infra, sections "连续批处理" and

@@ -236,6 +236,45 @@ class Allocator:
     def check(self):
         _check(lib().pkv_alloc_check(self._h), "check")
 
+    # -- prefix sharing --------------------------------------------------------
+    def match_prefix(self, req: int, namespace: int, tokens) -> int:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        return _check(lib().pkv_alloc_match_prefix(self._h, req, namespace, _ptr(t), len(t)),
+                      "match_prefix")
+
+    def peek_prefix(self, namespace: int, tokens) -> tuple[int, int]:
+        """(matched tokens, how many matched blocks are cached now)."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        cached = C.c_int32(0)
+        n = _check(lib().pkv_alloc_peek_prefix(self._h, namespace, _ptr(t), len(t),
+                                               C.byref(cached)), "peek_prefix")
+        return n, cached.value
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(lib().pkv_alloc_fork(self._h, parent, child), "fork")
+
+    def pending_copies(self) -> list[tuple[int, int]]:
+        buf = np.empty(2 * max(1, self.num_blocks), dtype=np.int32)
+        n = _check(lib().pkv_alloc_pending_copies(self._h, _ptr(buf), len(buf) // 2),
+                   "pending_copies")
+        return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n)]
+
+    def prefix_stats(self) -> dict:
+        s = _ffi.PrefixStats()
+        _check(lib().pkv_alloc_get_prefix_stats(self._h, C.byref(s)), "prefix_stats")
+        return {n: getattr(s, n) for n, _ in s._fields_}
+
+    def ref_count(self, block: int) -> int:
+        return _check(lib().pkv_alloc_ref_count(self._h, block), "ref_count")
+
+    def cached_list(self) -> list[int]:
+        buf = np.empty(self.num_blocks, dtype=np.int32)
+        n = _check(lib().pkv_alloc_cached_list(self._h, _ptr(buf), len(buf)), "cached_list")
+        return buf[:n].tolist()
+
+    def available(self) -> int:
+        return int(lib().pkv_alloc_available(self._h))
+
 
 class Scheduler:
     """Continuous-batching scheduler with recompute preemption (host)."""

@@ -29,6 +29,11 @@ class AllocStats(C.Structure):
                                    "tail_waste", "alloc_failures", "peak_used")]
 
 
+class PrefixStats(C.Structure):
+    _fields_ = [(n, i64) for n in ("lookups", "hits", "matched_tokens", "evictions", "cow_copies",
+                                   "indexed", "shared", "cached")]
+
+
 class SchedConfig(C.Structure):
     _fields_ = [("max_num_seqs", i32), ("max_num_batched_tokens", i32), ("chunk_size", i32),
                 ("max_model_len", i32), ("block_size", i32), ("num_blocks", i32),
@@ -74,6 +79,14 @@ SIGNATURES = {
     "pkv_alloc_held_tokens": (i64, [vp, i32]),
     "pkv_alloc_free_list": (C.c_int, [vp, vp, i32]),
     "pkv_alloc_check": (C.c_int, [vp]),
+    "pkv_alloc_match_prefix": (C.c_int, [vp, i32, u64, vp, i32]),
+    "pkv_alloc_peek_prefix": (C.c_int, [vp, u64, vp, i32, vp]),
+    "pkv_alloc_fork": (C.c_int, [vp, i32, i32]),
+    "pkv_alloc_pending_copies": (C.c_int, [vp, vp, i32]),
+    "pkv_alloc_get_prefix_stats": (C.c_int, [vp, C.POINTER(PrefixStats)]),
+    "pkv_alloc_ref_count": (C.c_int, [vp, i32]),
+    "pkv_alloc_cached_list": (C.c_int, [vp, vp, i32]),
+    "pkv_alloc_available": (i64, [vp]),
     "pkv_sched_create": (vp, [C.POINTER(SchedConfig)]),
     "pkv_sched_destroy": (None, [vp]),
     "pkv_sched_add_request": (C.c_int, [vp, i32, i32, i32]),

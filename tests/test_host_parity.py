@@ -164,3 +164,71 @@ def test_scheduler_small_random_with_faults(seed):
         _compare_step(cpp, ref, arrivals, fail_step=rng.random() < 0.1)
         cpp.allocator.check()
     assert cpp.counters()["inject_left"] == ref.inject_left
+
+
+def _same_prefix_alloc(cpp: pkv.Allocator, ref: NaiveAllocator, ids):
+    _same_alloc(cpp, ref, ids)
+    assert cpp.cached_list() == ref.cached
+    assert cpp.pending_copies() == ref.pending_copies()
+    assert cpp.available() == ref.available()
+    p, q = cpp.prefix_stats(), ref.prefix_stats()
+    assert (p["lookups"], p["hits"], p["matched_tokens"], p["evictions"], p["cow_copies"],
+            p["indexed"], p["shared"], p["cached"]) == \
+        (q.lookups, q.hits, q.matched_tokens, q.evictions, q.cow_copies, q.indexed, q.shared,
+         len(ref.cached))
+    for b in range(ref.capacity):
+        assert cpp.ref_count(b) == ref.ref_count(b)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_allocator_prefix_sharing_random_ops(seed):
+    """Prefix matching, forks, copy-on-write, eviction and the base
+    transitions, driven at random through both allocators."""
+    rng = random.Random(100 + seed)
+    B = rng.choice([2, 4, 16])
+    nb = rng.choice([12, 40, 96])
+    cpp, ref = pkv.Allocator(nb, B, 64), NaiveAllocator(nb, B, 64)
+    bases = [[rng.randrange(4) for _ in range(6 * B)] for _ in range(3)]
+    ids, live = [], []
+    nxt = 0
+    for _ in range(500):
+        op = rng.random()
+        if op < 0.25 and len(live) < 10:
+            ns = rng.randrange(2)
+            n = rng.randint(1, 6 * B)
+            toks = rng.choice(bases)[:n] if rng.random() < 0.75 else \
+                [rng.randrange(4) for _ in range(n)]
+            assert cpp.peek_prefix(ns, toks) == (len(ref.peek_prefix(ns, toks)) * B,
+                                                 sum(1 for b in ref.peek_prefix(ns, toks)
+                                                     if b in ref.cached))
+            assert cpp.match_prefix(nxt, ns, toks) == ref.match_prefix(nxt, ns, toks)
+            ids.append(nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.65 and live:
+            plan = [(r, rng.randint(0, 2 * B)) for r in rng.sample(live, rng.randint(1, min(4, len(live))))]
+            a, b = cpp.reserve(plan), ref.reserve(plan)
+            assert a == b
+            if a:
+                _same_prefix_alloc(cpp, ref, ids)
+                if rng.random() < 0.2:      # cancel one planned request mid-step
+                    r = rng.choice(plan)[0]
+                    assert cpp.free_request(r) == ref.free_request(r)
+                    live.remove(r)
+                if rng.random() < 0.8:
+                    cpp.commit(); ref.commit()
+                else:
+                    cpp.rollback(); ref.rollback()
+        elif op < 0.75 and live:
+            parent = rng.choice(live)
+            if ref.tables.get(parent):
+                cpp.fork(parent, nxt)
+                ref.fork(parent, nxt)
+                ids.append(nxt)
+                live.append(nxt)
+                nxt += 1
+        elif live:
+            r = rng.choice(live)
+            assert cpp.free_request(r) == ref.free_request(r)
+            live.remove(r)
+        _same_prefix_alloc(cpp, ref, ids)
