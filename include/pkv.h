@@ -132,6 +132,30 @@ int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t qu
                                void* stream);
 
 /* ------------------------------------------------------------------------
+ * copy_blocks  [显存调度, section "共享前缀会改变块的所有权": a shared block still
+ * being written is copied first (copy-on-write); 抢占 and [Chunked]: swapping
+ * moves a request's KV blocks between GPU and CPU memory]
+ *
+ * For i < num_pairs, with s = block_pairs[2i] and d = block_pairs[2i+1]:
+ *   dst_key_cache[d] = src_key_cache[s];  dst_value_cache[d] = src_value_cache[s]
+ * where a block is block_bytes contiguous bytes (block_size * num_kv_heads *
+ * head_dim * element size).  Source and destination may be the same pool
+ * (copy-on-write) or different ones, either in device memory or in mapped
+ * pinned host memory (the GPU reads and writes it over the CPU-GPU link).
+ * Destinations must be distinct, and within one pool no destination may
+ * also be a source, so the copies are independent.  A pair with s outside
+ * [0, src_num_blocks) or d outside [0, dst_num_blocks) is skipped and sets
+ * PKV_ERR_BLOCK_ID in *error_word (if not NULL).  The copy is bit-exact.
+ *
+ * block_pairs: int32 [num_pairs][2], device or mapped host memory.
+ * Pointers 16-byte aligned; block_bytes a positive multiple of 16.
+ * ---------------------------------------------------------------------- */
+int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void* dst_key_cache,
+                    void* dst_value_cache, const int32_t* block_pairs, int32_t num_pairs,
+                    int64_t src_num_blocks, int64_t dst_num_blocks, int64_t block_bytes,
+                    uint32_t* error_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * paged_attention_varlen  [AI Infra, section "Attention Module (以标准GQA +
  * RoPE为例)": attention per request over its whole K/V history read through
  * block_table, requests separated by query_start_loc (cu_seqlens); Flash-
@@ -223,6 +247,30 @@ int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t qu
                                int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                                int32_t head_dim, int32_t dtype, uint32_t* error_word,
                                void* stream);
+
+/* ------------------------------------------------------------------------
+ * copy_blocks  [显存调度, section "共享前缀会改变块的所有权": a shared block still
+ * being written is copied first (copy-on-write); 抢占 and [Chunked]: swapping
+ * moves a request's KV blocks between GPU and CPU memory]
+ *
+ * For i < num_pairs, with s = block_pairs[2i] and d = block_pairs[2i+1]:
+ *   dst_key_cache[d] = src_key_cache[s];  dst_value_cache[d] = src_value_cache[s]
+ * where a block is block_bytes contiguous bytes (block_size * num_kv_heads *
+ * head_dim * element size).  Source and destination may be the same pool
+ * (copy-on-write) or different ones, either in device memory or in mapped
+ * pinned host memory (the GPU reads and writes it over the CPU-GPU link).
+ * Destinations must be distinct, and within one pool no destination may
+ * also be a source, so the copies are independent.  A pair with s outside
+ * [0, src_num_blocks) or d outside [0, dst_num_blocks) is skipped and sets
+ * PKV_ERR_BLOCK_ID in *error_word (if not NULL).  The copy is bit-exact.
+ *
+ * block_pairs: int32 [num_pairs][2], device or mapped host memory.
+ * Pointers 16-byte aligned; block_bytes a positive multiple of 16.
+ * ---------------------------------------------------------------------- */
+int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void* dst_key_cache,
+                    void* dst_value_cache, const int32_t* block_pairs, int32_t num_pairs,
+                    int64_t src_num_blocks, int64_t dst_num_blocks, int64_t block_bytes,
+                    uint32_t* error_word, void* stream);
 
 /* ------------------------------------------------------------------------
  * paged_attention_varlen without a workspace.  The pages have no counterpart:
@@ -446,6 +494,13 @@ void pkv_sched_destroy(pkv_sched* s);
  * footprint that can never fit); the output target is clamped to
  * max_model_len - prompt_len */
 int pkv_sched_add_request(pkv_sched* s, int32_t req_id, int32_t prompt_len, int32_t max_output);
+/* As pkv_sched_add_request, with the prompt's token ids tokens[0..prompt_len)
+ * in namespace ns: on admission the request is matched against the prefix
+ * index (pkv_alloc_match_prefix) and starts at the matched token count; its
+ * full prompt blocks are indexed as they are committed.  Returns 1 if
+ * queued, 0 if rejected. */
+int pkv_sched_add_request_tokens(pkv_sched* s, int32_t req_id, int32_t prompt_len,
+                                 int32_t max_output, uint64_t ns, const int32_t* tokens);
 int pkv_sched_step(pkv_sched* s, pkv_step_info* info);
 /* plan entries, in batch order */
 int pkv_sched_plan(const pkv_sched* s, int32_t* req_ids, int32_t* num_new_tokens,

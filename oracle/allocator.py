@@ -274,16 +274,23 @@ class NaiveAllocator:
         else:
             self.free_list.append(b)
 
-    def _evict_one(self) -> None:
-        parents = {key[1] for key in self.index}
-        for b in self.cached:
-            if b not in parents:
-                self.cached.remove(b)
-                del self.index[self.key_of.pop(b)]
-                self.free_list.append(b)
-                self.pfx.evictions += 1
-                return
-        raise AllocatorError("no evictable cached block")
+    def _evict(self, n: int) -> None:
+        """Evict n cached blocks, each time the oldest one no indexed block extends."""
+        children: dict[int, int] = {}
+        for key in self.index:
+            children[key[1]] = children.get(key[1], 0) + 1
+        for _ in range(n):
+            for b in self.cached:
+                if children.get(b, 0) == 0:
+                    break
+            else:
+                raise AllocatorError("no evictable cached block")
+            self.cached.remove(b)
+            key = self.key_of.pop(b)
+            del self.index[key]
+            children[key[1]] -= 1
+            self.free_list.append(b)
+            self.pfx.evictions += 1
 
     # -- transitions -------------------------------------------------------------
     def fork(self, parent: int, child: int) -> None:
@@ -309,6 +316,10 @@ class NaiveAllocator:
         need, cows = [], []
         B = self.block_size
         copied_away: dict[int, int] = {}   # source block -> earlier plan entries copying it
+        holders: dict[int, int] = {}       # block -> requests holding it
+        for t in self.tables.values():
+            for b in t:
+                holders[b] = holders.get(b, 0) + 1
         for r, s in plan:
             if s < 0:
                 raise AllocatorError("negative token count")
@@ -320,7 +331,7 @@ class NaiveAllocator:
             if s > 0 and held % B != 0:
                 last = self.tables[r][-1]
                 # the last writer of a shared partial block keeps the original
-                cow = self.holders(last) - copied_away.get(last, 0) > 1
+                cow = holders[last] - copied_away.get(last, 0) > 1
                 if cow:
                     copied_away[last] = copied_away.get(last, 0) + 1
             need.append(d)
@@ -329,8 +340,8 @@ class NaiveAllocator:
         if total > self.available():
             self.alloc_failures += 1
             return False
-        while len(self.free_list) < total:
-            self._evict_one()
+        if len(self.free_list) < total:
+            self._evict(total - len(self.free_list))
         pending = []
         for (r, s), d, cow in zip(plan, need, cows):
             c = None

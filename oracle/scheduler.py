@@ -41,6 +41,18 @@ Readings where the pages are silent (all stated in the design notes):
 * add_request clamps the output target to max_model_len - prompt_len and
   rejects a request whose largest footprint exceeds the pool or its block
   table, so no request can loop on self-preemption forever.
+
+Prefix sharing ("显存与调度", sections "共享前缀会改变块的所有权" and "内存压力需要
+明确策略"; "Chunked Prefill 与 Preemption": a prefix cache can let a
+recomputed request hit part of its prefix):
+* a request added with its prompt's token ids (and a namespace) is matched
+  against the allocator's prefix index when it is admitted: it starts with
+  the matched blocks and num_computed = the matched token count, and its
+  full prompt blocks are indexed as they are committed;
+* the blocks a step may take are q_free + q_cached (cached prefix blocks are
+  evicted on demand); an admitted request's first chunk fits when its new
+  blocks plus the cached blocks its match takes out of the cache fit; a
+  preemption gives back the blocks no other request holds.
 """
 
 from __future__ import annotations
@@ -87,6 +99,8 @@ class Request:
     outputs: int = 0
     status: str = WAITING
     preemptions: int = 0
+    namespace: int = 0
+    tokens: list | None = None    # prompt token ids, for prefix sharing
 
 
 @dataclass
@@ -112,15 +126,20 @@ class NaiveScheduler:
         self.recomputed_tokens = 0
 
     # -- requests ------------------------------------------------------------------
-    def add_request(self, rid: int, prompt_len: int, max_output: int) -> bool:
+    def add_request(self, rid: int, prompt_len: int, max_output: int, namespace: int = 0,
+                    tokens=None) -> bool:
         c = self.cfg
         if rid in self.reqs or prompt_len < 1 or max_output < 1 or prompt_len >= c.max_model_len:
+            return False
+        if tokens is not None and len(tokens) != prompt_len:
             return False
         max_output = min(max_output, c.max_model_len - prompt_len)
         largest = blocks_for(prompt_len + max_output, c.block_size)
         if largest > c.num_blocks or largest > c.max_blocks_per_req:
             return False
-        self.reqs[rid] = Request(rid, prompt_len, max_output, num_tokens=prompt_len)
+        self.reqs[rid] = Request(rid, prompt_len, max_output, num_tokens=prompt_len,
+                                 namespace=namespace,
+                                 tokens=None if tokens is None else [int(t) for t in tokens])
         self.waiting.append(rid)
         return True
 
@@ -129,10 +148,11 @@ class NaiveScheduler:
         self.rng_state, z = splitmix64_next(self.rng_state)
         return (z >> 11) * (1.0 / (1 << 53))
 
-    def _preempt(self, rid: int, plan: StepPlan) -> None:
+    def _preempt(self, rid: int, plan: StepPlan) -> int:
+        """Recompute preemption; returns the blocks no request holds any more."""
         req = self.reqs[rid]
         self.recomputed_tokens += req.num_computed
-        self.alloc.free_request(rid)
+        released = self.alloc.free_request(rid)
         req.num_computed = 0
         req.status = WAITING
         req.preemptions += 1
@@ -140,6 +160,7 @@ class NaiveScheduler:
         self.running.remove(rid)
         self.waiting.insert(0, rid)
         plan.preempted.append(rid)
+        return released
 
     def step(self) -> StepPlan:
         if self.plan is not None:
@@ -148,7 +169,7 @@ class NaiveScheduler:
         B = c.block_size
         plan = StepPlan()
         budget = c.max_num_batched_tokens
-        free = self.alloc.num_free()
+        free = self.alloc.available()
         wanted = []   # (rid, s)
 
         # RUNNING, head first; victims come from the unscheduled tail
@@ -171,12 +192,9 @@ class NaiveScheduler:
                 if fits:
                     break
                 if i + 1 < len(self.running):
-                    victim = self.running[-1]
-                    free += len(self.alloc.table(victim))
-                    self._preempt(victim, plan)
+                    free += self._preempt(self.running[-1], plan)
                 else:
-                    free += len(self.alloc.table(rid))
-                    self._preempt(rid, plan)
+                    free += self._preempt(rid, plan)
                     scheduled = False
                     break
             if not scheduled:
@@ -191,17 +209,25 @@ class NaiveScheduler:
             while self.waiting and budget > 0 and len(self.running) < c.max_num_seqs:
                 rid = self.waiting[0]
                 req = self.reqs[rid]
-                s = min(req.num_tokens - req.num_computed, c.chunk_size, budget)
-                need = delta_blocks(self.alloc.held_tokens(rid), s, B)
-                if need > free:
+                matched, from_cache = 0, 0
+                prefix = req.tokens is not None and req.num_computed == 0
+                if prefix:
+                    blocks = self.alloc.peek_prefix(req.namespace, req.tokens)
+                    matched = len(blocks) * B
+                    from_cache = sum(1 for b in blocks if b in self.alloc.cached)
+                s = min(req.num_tokens - max(req.num_computed, matched), c.chunk_size, budget)
+                need = delta_blocks(max(self.alloc.held_tokens(rid), matched), s, B)
+                if need + from_cache > free:
                     break
+                if prefix:
+                    req.num_computed = self.alloc.match_prefix(rid, req.namespace, req.tokens)
                 self.waiting.pop(0)
                 self.running.append(rid)
                 req.status = RUNNING
                 plan.admitted.append(rid)
                 wanted.append((rid, s))
                 budget -= s
-                free -= need
+                free -= need + from_cache
 
         for rid, s in wanted:
             plan.entries.append((rid, s, self.reqs[rid].num_computed))

@@ -18,7 +18,8 @@ from ._ffi import (ERR_BLOCK_ID, ERR_METADATA, ERR_POSITION, ERR_SLOT, ERR_TIMEO
                    PKV_BF16, PKV_F32)
 
 __all__ = [
-    "PkvError", "lib", "reshape_and_cache", "rope_reshape_and_cache", "attention_workspace_bytes", "new_workspace",
+    "PkvError", "lib", "reshape_and_cache", "rope_reshape_and_cache", "copy_blocks",
+    "attention_workspace_bytes", "new_workspace",
     "paged_attention_varlen", "read_error_word", "build_slot_mapping", "Allocator", "Scheduler",
 ]
 
@@ -114,6 +115,26 @@ def rope_reshape_and_cache(positions, query, key, value, key_cache, value_cache,
         int(bool(is_neox)), int(positions.shape[0]), nb, bs, hkv, d, _dtype_code(key_cache),
         error_word.data_ptr() if error_word is not None else None, _stream_ptr(stream))
     _check(code, "rope_reshape_and_cache")
+
+
+def copy_blocks(src_key_cache, src_value_cache, dst_key_cache, dst_value_cache, block_pairs,
+                error_word=None, stream=None) -> None:
+    """Copy whole blocks: dst[pairs[i, 1]] = src[pairs[i, 0]] for K and V.  Pools are
+    [num_blocks, block_size, Hkv, D] tensors (device, or pinned host memory the
+    device can map); block_pairs is int32 [n, 2] (device or pinned host)."""
+    for t in (src_key_cache, src_value_cache, dst_key_cache, dst_value_cache, block_pairs):
+        if not t.is_contiguous():
+            raise ValueError("pools and block_pairs must be contiguous")
+    if src_key_cache.shape[1:] != dst_key_cache.shape[1:] or \
+            src_key_cache.dtype != dst_key_cache.dtype:
+        raise ValueError("source and destination pools must have the same block shape and dtype")
+    block_bytes = src_key_cache[0].numel() * src_key_cache.element_size()
+    code = lib().pkv_copy_blocks(
+        src_key_cache.data_ptr(), src_value_cache.data_ptr(), dst_key_cache.data_ptr(),
+        dst_value_cache.data_ptr(), block_pairs.data_ptr(), int(block_pairs.shape[0]),
+        int(src_key_cache.shape[0]), int(dst_key_cache.shape[0]), block_bytes,
+        error_word.data_ptr() if error_word is not None else None, _stream_ptr(stream))
+    _check(code, "copy_blocks")
 
 
 def attention_workspace_bytes(num_reqs: int, num_heads: int, head_dim: int) -> int:
@@ -298,9 +319,19 @@ class Scheduler:
             lib().pkv_sched_destroy(self._h)
             self._h = None
 
-    def add_request(self, req_id: int, prompt_len: int, max_output: int) -> bool:
-        return bool(_check(lib().pkv_sched_add_request(self._h, req_id, prompt_len, max_output),
-                           "add_request"))
+    def add_request(self, req_id: int, prompt_len: int, max_output: int, namespace: int = 0,
+                    tokens=None) -> bool:
+        """Queue a request; with `tokens` (its prompt's token ids) it takes part in
+        prefix sharing within `namespace`."""
+        if tokens is None:
+            code = lib().pkv_sched_add_request(self._h, req_id, prompt_len, max_output)
+        else:
+            t = np.ascontiguousarray(tokens, dtype=np.int32)
+            if len(t) != prompt_len:
+                return False
+            code = lib().pkv_sched_add_request_tokens(self._h, req_id, prompt_len, max_output,
+                                                      namespace, _ptr(t))
+        return bool(_check(code, "add_request"))
 
     def step(self) -> dict:
         _check(lib().pkv_sched_step(self._h, C.byref(self.info)), "step")

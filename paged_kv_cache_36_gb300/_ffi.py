@@ -60,6 +60,7 @@ SIGNATURES = {
     "pkv_rope_reshape_and_cache": (C.c_int, [vp, vp, i64, i32, vp, i64, vp, vp, i64, vp, vp,
                                              vp, vp, i64, i32, i32, i64, i64, i32, i32, i32,
                                              i32, vp, vp]),
+    "pkv_copy_blocks": (C.c_int, [vp, vp, vp, vp, vp, i32, i64, i64, i64, vp, vp]),
     "pkv_attention_workspace_bytes": (sz, [i32, i32, i32]),
     "pkv_paged_attention_varlen": (C.c_int, [vp, i64, vp, vp, vp, i32, vp, vp, vp, f32, vp, i64,
                                              i64, i32, i64, i32, i32, i32, i32, i32, i32, vp, sz,
@@ -90,6 +91,7 @@ SIGNATURES = {
     "pkv_sched_create": (vp, [C.POINTER(SchedConfig)]),
     "pkv_sched_destroy": (None, [vp]),
     "pkv_sched_add_request": (C.c_int, [vp, i32, i32, i32]),
+    "pkv_sched_add_request_tokens": (C.c_int, [vp, i32, i32, i32, u64, vp]),
     "pkv_sched_step": (C.c_int, [vp, C.POINTER(StepInfo)]),
     "pkv_sched_plan": (C.c_int, [vp, vp, vp, vp, i32]),
     "pkv_sched_preempted": (C.c_int, [vp, vp, i32]),

@@ -251,6 +251,26 @@ int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t qu
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "rope_reshape_and_cache launch");
 }
 
+int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void* dst_key_cache,
+                    void* dst_value_cache, const int32_t* block_pairs, int32_t num_pairs,
+                    int64_t src_num_blocks, int64_t dst_num_blocks, int64_t block_bytes,
+                    uint32_t* error_word, void* stream) {
+  if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_bytes <= 0 ||
+      block_bytes % 16)
+    return fail(PKV_E_INVALID, "pkv_copy_blocks: bad sizes");
+  if (num_pairs == 0) return PKV_OK;
+  if (!src_key_cache || !src_value_cache || !dst_key_cache || !dst_value_cache || !block_pairs)
+    return fail(PKV_E_INVALID, "pkv_copy_blocks: null pointer");
+  if (!aligned16(src_key_cache) || !aligned16(src_value_cache) || !aligned16(dst_key_cache) ||
+      !aligned16(dst_value_cache))
+    return fail(PKV_E_INVALID, "pkv_copy_blocks: pools must be 16-byte aligned");
+  cudaError_t e = launch_copy_blocks(src_key_cache, src_value_cache, dst_key_cache,
+                                     dst_value_cache, block_pairs, num_pairs, block_bytes,
+                                     src_num_blocks, dst_num_blocks, error_word,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "copy_blocks launch");
+}
+
 size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_t head_dim) {
   if (num_reqs < 0 || num_heads <= 0 || head_dim <= 0) return 0;
   return workspace_layout(num_reqs, num_heads, head_dim, current_grid()).total;

@@ -18,6 +18,14 @@
 //   reservation, commit/rollback) and "分块预填充共享每轮预算" (sum of the
 //   step's decode and chunk tokens <= K).
 //
+// * "显存与调度", sections "共享前缀会改变块的所有权" and "内存压力需要明确策略";
+//   "Chunked Prefill 与 Preemption" (a prefix cache lets a recomputed request
+//   hit part of its prefix): a request added with its prompt's token ids is
+//   matched against the prefix index when admitted and starts at the matched
+//   token count; a step may take q_free + q_cached blocks (cached ones are
+//   evicted on demand); a preemption gives back the blocks no other request
+//   holds.
+//
 // Where the pages leave a step open this follows the same readings as the
 // library's design notes: s_i = min(num_tokens - num_computed, chunk_size,
 // remaining budget); a request that catches up samples one token and then
@@ -59,6 +67,9 @@ struct Req {
   int64_t num_computed = 0;
   int32_t preemptions = 0;
   Status status = kWaiting;
+  bool has_tokens = false;      // prompt token ids known: prefix sharing applies
+  uint64_t ns = 0;
+  std::vector<int32_t> tokens;
 };
 
 struct Entry {
@@ -73,7 +84,8 @@ class Scheduler {
       : cfg_(c), handle_(c.num_blocks, c.block_size, c.max_blocks_per_req), alloc_(handle_.impl),
         rng_{c.artificial_seed}, inject_left_(c.artificial_preempt_max) {}
 
-  int add_request(int32_t id, int32_t prompt, int32_t max_output) {
+  int add_request(int32_t id, int32_t prompt, int32_t max_output, uint64_t ns = 0,
+                  const int32_t* tokens = nullptr) {
     if (reqs_.count(id) || prompt < 1 || max_output < 1 || prompt >= cfg_.max_model_len) return 0;
     max_output = std::min<int32_t>(max_output, cfg_.max_model_len - prompt);
     const int64_t largest = ceil_div64(static_cast<int64_t>(prompt) + max_output, cfg_.block_size);
@@ -83,7 +95,12 @@ class Scheduler {
     r.prompt_len = prompt;
     r.max_output = max_output;
     r.num_tokens = prompt;
-    reqs_.emplace(id, r);
+    if (tokens) {
+      r.has_tokens = true;
+      r.ns = ns;
+      r.tokens.assign(tokens, tokens + prompt);
+    }
+    reqs_.emplace(id, std::move(r));
     waiting_.push_back(id);
     return 1;
   }
@@ -95,7 +112,7 @@ class Scheduler {
     admitted_.clear();
     const int32_t B = cfg_.block_size;
     int64_t budget = cfg_.max_num_batched_tokens;
-    int64_t free_blocks = alloc_.num_free();
+    int64_t free_blocks = alloc_.available();
 
     // RUNNING scan, head first.  Requests before position i are scheduled;
     // victims are taken from the back, which is never before i.
@@ -137,17 +154,28 @@ class Scheduler {
       while (!waiting_.empty() && budget > 0 &&
              static_cast<int64_t>(running_.size()) < cfg_.max_num_seqs) {
         Req& r = reqs_.at(waiting_.front());
-        const int64_t s = std::min<int64_t>({r.num_tokens - r.num_computed, cfg_.chunk_size, budget});
-        const int64_t held = alloc_.held_tokens(r.id);
+        int64_t matched = 0;
+        int32_t from_cache = 0;
+        const bool prefix = r.has_tokens && r.num_computed == 0;
+        if (prefix)
+          matched = alloc_.peek_prefix(r.ns, r.tokens.data(), r.prompt_len, &from_cache);
+        const int64_t start = std::max(r.num_computed, matched);
+        const int64_t s = std::min<int64_t>({r.num_tokens - start, cfg_.chunk_size, budget});
+        const int64_t held = std::max(alloc_.held_tokens(r.id), matched);
         const int64_t need = ceil_div64(held + s, B) - ceil_div64(held, B);
-        if (need > free_blocks) break;
+        if (need + from_cache > free_blocks) break;
+        if (prefix) {
+          const int m = alloc_.match_prefix(r.id, r.ns, r.tokens.data(), r.prompt_len);
+          if (m < 0) return m;
+          r.num_computed = m;
+        }
         waiting_.pop_front();
         running_.push_back(r.id);
         r.status = kRunning;
         admitted_.push_back(r.id);
         entries_.push_back({r.id, static_cast<int32_t>(s), r.num_computed});
         budget -= s;
-        free_blocks -= need;
+        free_blocks -= need + from_cache;
       }
     }
 
@@ -316,6 +344,13 @@ void pkv_sched_destroy(pkv_sched* s) { delete s; }
 int pkv_sched_add_request(pkv_sched* s, int32_t id, int32_t prompt, int32_t max_output) {
   PKV_NEED_S(s);
   return s->impl.add_request(id, prompt, max_output);
+}
+
+int pkv_sched_add_request_tokens(pkv_sched* s, int32_t id, int32_t prompt, int32_t max_output,
+                                 uint64_t ns, const int32_t* tokens) {
+  PKV_NEED_S(s);
+  if (!tokens) return fail(PKV_E_INVALID, "pkv_sched_add_request_tokens: null tokens");
+  return s->impl.add_request(id, prompt, max_output, ns, tokens);
 }
 
 int pkv_sched_step(pkv_sched* s, pkv_step_info* info) {

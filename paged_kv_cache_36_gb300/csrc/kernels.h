@@ -95,6 +95,13 @@ struct RopeArgs {
 
 cudaError_t launch_rope_reshape_and_cache(const RopeArgs& a, cudaStream_t stream);
 
+// Whole-block copies of K and V between two pools (or within one): block
+// pairs[2i] of the source pool to block pairs[2i+1] of the destination pool.
+cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                               const int32_t* pairs, int32_t n, int64_t block_bytes,
+                               int64_t src_blocks, int64_t dst_blocks, uint32_t* err,
+                               cudaStream_t stream);
+
 // Grid size (CTAs) of the persistent split-KV decode kernel on this device.
 int decode_grid_size(int device);
 

@@ -11,7 +11,7 @@ import paged_kv_cache_36_gb300 as pkv
 from oracle import paging
 from oracle.allocator import NaiveAllocator
 from oracle.scheduler import NaiveScheduler, SchedConfig
-from workloads import generate_arrivals, trace_spec
+from workloads import generate_arrivals, generate_prefix_arrivals, trace_spec
 
 
 def _same_alloc(cpp: pkv.Allocator, ref: NaiveAllocator, ids):
@@ -100,8 +100,12 @@ def _pair(c: SchedConfig):
 
 def _compare_step(cpp, ref, arrivals_now, fail_step=False, check_tables=True):
     for a in arrivals_now:
-        assert cpp.add_request(a.req_id, a.prompt_len, a.max_output) == \
-            ref.add_request(a.req_id, a.prompt_len, a.max_output)
+        if getattr(a, "tokens", ()):
+            assert cpp.add_request(a.req_id, a.prompt_len, a.max_output, a.namespace, a.tokens) == \
+                ref.add_request(a.req_id, a.prompt_len, a.max_output, a.namespace, a.tokens)
+        else:
+            assert cpp.add_request(a.req_id, a.prompt_len, a.max_output) == \
+                ref.add_request(a.req_id, a.prompt_len, a.max_output)
     pc = cpp.step()
     pr = ref.step()
     assert pc["entries"] == pr.entries
@@ -232,3 +236,34 @@ def test_allocator_prefix_sharing_random_ops(seed):
             assert cpp.free_request(r) == ref.free_request(r)
             live.remove(r)
         _same_prefix_alloc(cpp, ref, ids)
+
+
+def test_scheduler_prefix_trace_bit_exact():
+    """The 300-step trace with shared system prompts in two namespaces: the
+    C++ scheduler and allocator against the oracle's, step by step, including
+    the prefix index's statistics."""
+    spec = trace_spec()
+    c = SchedConfig(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                    spec.max_model_len, spec.block_size, spec.num_blocks,
+                    spec.max_model_len // spec.block_size)
+    cpp, ref = _pair(c)
+    by_step = {}
+    for a in generate_prefix_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    for step in range(spec.steps):
+        _compare_step(cpp, ref, by_step.get(step, []), check_tables=(step % 10 == 0))
+        if step % 10 == 0:
+            p, q = cpp.allocator.prefix_stats(), ref.alloc.prefix_stats()
+            assert (p["lookups"], p["hits"], p["matched_tokens"], p["evictions"], p["indexed"],
+                    p["shared"], p["cached"]) == \
+                (q.lookups, q.hits, q.matched_tokens, q.evictions, q.indexed, q.shared,
+                 len(ref.alloc.cached))
+            assert cpp.allocator.cached_list() == ref.alloc.cached
+        if step % 25 == 0:
+            cpp.allocator.check()
+            ref.alloc.deep_check()
+    q = ref.alloc.prefix_stats()
+    assert q.hits > 100 and q.matched_tokens > 100000     # sharing actually happens
+    cnt = cpp.counters()
+    assert cnt["preemptions"] == ref.total_preemptions
+    assert cnt["recomputed_tokens"] == ref.recomputed_tokens

@@ -24,4 +24,4 @@ from .configs import (  # noqa: F401
     tiny_fp32_case,
     trace_spec,
 )
-from .trace import Arrival, generate_arrivals  # noqa: F401
+from .trace import Arrival, PrefixArrival, generate_arrivals, generate_prefix_arrivals  # noqa: F401
