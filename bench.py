@@ -481,6 +481,83 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     }
     del prompts
     torch.cuda.empty_cache()
+    # ---- whole-block copies: copy-on-write within the pool, offload to and
+    # reload from pinned host memory (the GPU drives the CPU-GPU link) ----
+    nbp, n = 16384, 4096
+    kc = torch.randn((nbp, 16, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    vc = torch.randn((nbp, 16, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    hk = torch.empty((n, 16, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    blk = random_block_placement(nbp, [2 * n], "bench", "copy blocks")[0].astype(np.int32)
+    cow = torch.from_numpy(np.stack([blk[:n], blk[n:]], axis=1)).to(device)
+    out_p = torch.from_numpy(np.stack([blk[:n], np.arange(n, dtype=np.int32)], axis=1)).to(device)
+    in_p = torch.from_numpy(np.stack([np.arange(n, dtype=np.int32), blk[n:]], axis=1)).to(device)
+    copy_bytes = 2 * n * 16 * Hkv * D * 2   # K and V blocks moved
+    res_copy = {"workload": "4096 scattered blocks of Llama-3-8B shape (K+V, 256 MiB moved), "
+                            "from a 16384-block pool", "bytes_per_call": copy_bytes}
+    for name, args in (("device_to_device", (kc, vc, kc, vc, cow)),
+                       ("device_to_host", (kc, vc, hk, hv, out_p)),
+                       ("host_to_device", (hk, hv, kc, vc, in_p))):
+        for _ in range(3):
+            pkv.copy_blocks(*args)
+        ms = event_time(lambda: pkv.copy_blocks(*args), 10, stream)
+        res_copy[name] = {"ms": ms, "gbs": copy_bytes / (ms * 1e-3) / 1e9}
+    res_copy["device_to_device"]["frac_of_hbm_peak"] = \
+        2 * copy_bytes / (res_copy["device_to_device"]["ms"] * 1e-3) / 1e9 / hbm_peak
+    res["copy_blocks"] = res_copy
+    del kc, vc, hk, hv
+    torch.cuda.empty_cache()
+    # ---- the trace with shared system prompts (prefix sharing on) ----
+    from workloads import generate_prefix_arrivals
+    spec = trace_spec()
+    H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    sched = pkv.Scheduler(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                          spec.max_model_len, B, spec.num_blocks, spec.max_model_len // B)
+    kc = torch.zeros((spec.num_blocks, B, Hkv, D), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    ws = pkv.new_workspace(spec.max_num_seqs, H, D, device)
+    budget = spec.max_num_batched_tokens
+    qp = torch.randn((budget, H, D), generator=g, device=device).to(torch.bfloat16)
+    kp = torch.randn((budget, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    vp = torch.randn((budget, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    by_step = {}
+    for a in generate_prefix_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    toks_done, ms_total = 0, 0.0
+    for st in range(spec.steps):
+        for a in by_step.get(st, []):
+            sched.add_request(a.req_id, a.prompt_len, a.max_output, a.namespace, a.tokens)
+        plan = sched.step()
+        bt, qsl, seq, nc, slots = sched.metadata()
+        T = int(qsl[-1])
+        if T:
+            dev = [torch.from_numpy(x).to(device) for x in (bt, qsl, seq, nc, slots)]
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            pkv.reshape_and_cache(kp[:T], vp[:T], kc, vc, dev[4])
+            pkv.paged_attention_varlen(qp[:T], kc, vc, dev[0], dev[1], dev[2], dev[3],
+                                       1.0 / math.sqrt(D), workspace=ws,
+                                       max_query_len=plan["max_query_len"])
+            b_ev.record(stream)
+            b_ev.synchronize()
+            toks_done += T
+            ms_total += a_ev.elapsed_time(b_ev)
+        sched.finish_step(True)
+    pst = sched.allocator.prefix_stats()
+    res["prefix_trace"] = {
+        "workload": "300-step trace, 75 % of prompts = one of 8 shared system prompts "
+                    "(popularity 1/(k+1), median 1536 tokens, 2 namespaces) + a private part "
+                    "(median 256), C++ scheduler with the prefix index, 16384-block pool",
+        "tokens_computed": toks_done, "prefix_tokens_matched": int(pst["matched_tokens"]),
+        "lookups": int(pst["lookups"]), "hits": int(pst["hits"]),
+        "evictions": int(pst["evictions"]),
+        "tokens_per_s_per_layer": toks_done / (ms_total * 1e-3),
+        "prompt_tokens_served_per_s_per_layer": (toks_done + pst["matched_tokens"]) / (ms_total * 1e-3),
+        "preemptions": int(sched.counters()["preemptions"]),
+        "timing": "CUDA events around reshape_and_cache + paged_attention_varlen of each step",
+    }
+    del kc, vc, ws, sched
+    torch.cuda.empty_cache()
     # ---- config 5: the trace, per step (C++ scheduler, device-random K/V/Q) ----
     spec = trace_spec()
     H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size

@@ -99,3 +99,92 @@ def test_trace_300_steps():
     torch.cuda.synchronize()
     assert pkv.read_error_word(ws) == 0
     assert preemptions > 0 and checked >= spec.steps // CHECK_EVERY - 1
+
+
+def test_prefix_sharing_trace_300_steps():
+    """The trace with shared system prompts (8 prompts, two namespaces): the
+    schedulers match prompts against the prefix index, so requests read
+    blocks another request wrote.  K/V rows are a function of the content
+    that fixes them - (namespace, system prompt, position) inside a shared
+    system prompt, (request, position) elsewhere - as a real model's would
+    be.  Every CHECK_EVERY-th step up to 24 requests (those starting from a
+    matched prefix first) are compared with the float64 oracle over their
+    logical histories."""
+    import paged_kv_cache_36_gb300 as pkv
+    from workloads import generate_prefix_arrivals
+    spec = trace_spec()
+    H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    mbpr = spec.max_model_len // B
+    c = SchedConfig(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                    spec.max_model_len, B, spec.num_blocks, mbpr)
+    ref = NaiveScheduler(c, deep_checks=False)
+    cpp = pkv.Scheduler(c.max_num_seqs, c.max_num_batched_tokens, c.chunk_size, c.max_model_len,
+                        B, c.num_blocks, mbpr)
+    kv_rows = PooledRows(Hkv * D, "prefix_kv")
+    q_rows = PooledRows(H * D, "prefix_q")
+    kc = torch.zeros(spec.num_blocks, B, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ws = pkv.new_workspace(spec.max_num_seqs, H, D)
+    arrivals = generate_prefix_arrivals(spec)
+    info = {a.req_id: a for a in arrivals}
+    by_step = {}
+    for a in arrivals:
+        by_step.setdefault(a.step, []).append(a)
+
+    def content(rid, pos):
+        a = info[rid]
+        key = np.full(len(pos), rid, dtype=np.int64)
+        if a.system >= 0:
+            key[pos < a.system_len] = (1 << 20) + a.namespace * 64 + a.system
+        return key
+
+    def history(rid, n):
+        pos = np.arange(n)
+        k = content(rid, pos)
+        return kv_rows.rows(0, k, pos).view(n, Hkv, D), kv_rows.rows(1, k, pos).view(n, Hkv, D)
+
+    checked = matched_reqs = 0
+    for step in range(spec.steps):
+        for a in by_step.get(step, []):
+            assert cpp.add_request(a.req_id, a.prompt_len, a.max_output, a.namespace, a.tokens) == \
+                ref.add_request(a.req_id, a.prompt_len, a.max_output, a.namespace, a.tokens)
+        pc, pr = cpp.step(), ref.step()
+        assert pc["entries"] == pr.entries and pc["preempted"] == pr.preempted
+        assert pc["admitted"] == pr.admitted
+        bt, qsl, seq, nc, slots = cpp.metadata()
+        rqsl, rseq, rnc, rrows, rslots = ref.metadata(pr)
+        assert qsl.tolist() == rqsl and seq.tolist() == rseq and nc.tolist() == rnc
+        assert slots.tolist() == rslots
+        for k, row in enumerate(rrows):
+            assert bt[k, :len(row)].tolist() == row
+        T = int(qsl[-1])
+        if T:
+            rid_of = np.repeat([e[0] for e in pr.entries], [e[1] for e in pr.entries])
+            pos = np.concatenate([np.arange(e[2], e[2] + e[1]) for e in pr.entries])
+            keys = np.concatenate([content(r, np.arange(e2, e2 + s)) for r, s, e2 in pr.entries])
+            assert len(keys) == len(pos) == len(rid_of)
+            kn = kv_rows.rows(0, keys, pos).view(T, Hkv, D)
+            vn = kv_rows.rows(1, keys, pos).view(T, Hkv, D)
+            q = q_rows.rows(2, np.full(T, step), np.arange(T)).view(T, H, D)
+            pkv.reshape_and_cache(kn.cuda(), vn.cuda(), kc, vc, torch.from_numpy(slots).cuda())
+            out = pkv.paged_attention_varlen(
+                q.cuda(), kc, vc, torch.from_numpy(bt).cuda(), torch.from_numpy(qsl).cuda(),
+                torch.from_numpy(seq).cuda(), torch.from_numpy(nc).cuda(), 1.0 / math.sqrt(D),
+                workspace=ws, max_query_len=pc["max_query_len"])
+            matched_reqs += sum(1 for r in pr.admitted if ref.reqs[r].num_computed > 0)
+            if step % CHECK_EVERY == 0:
+                R = len(pr.entries)
+                order = sorted(range(R), key=lambda k: (pr.entries[k][2] == 0, k))
+                pick = sorted(order[:24])
+                histories = [history(pr.entries[k][0], int(seq[k])) if k in pick else None
+                             for k in range(R)]
+                want = oa.paged_attention_varlen(q, histories, qsl, seq, nc, 1.0 / math.sqrt(D),
+                                                 rows=pick)
+                compare(out, want, qsl, torch.bfloat16, rows=pick)
+                assert pkv.read_error_word(ws) == 0
+                checked += 1
+        assert cpp.finish_step(True) == ref.finish_step(True)
+    torch.cuda.synchronize()
+    assert pkv.read_error_word(ws) == 0
+    st = cpp.allocator.prefix_stats()
+    assert st["hits"] > 100 and matched_reqs > 50 and checked >= spec.steps // CHECK_EVERY - 1
