@@ -61,6 +61,26 @@ Readings where that section is silent:
   plan order, a request copies only while some other holder of the block has
   not already copied it away in the same plan: the last writer keeps the
   original.
+
+Swapping ("vLLM 抢占机制源码精读", sections "Swap 模式" and "Swap-in 恢复流程";
+"GPT-5 时代大模型推理调度系统深度实战", section 4.3):
+* swap_out moves a request's KV blocks to a CPU block pool: it needs a free
+  CPU block per GPU block (can_swap_out), returns the GPU -> CPU mapping for
+  the data transfer, and releases the GPU blocks at once;
+* swap_in is the reverse: GPU blocks for every CPU block, the CPU -> GPU
+  mapping, and the CPU blocks are released; it is "never" possible when the
+  request has more blocks than the GPU pool, "later" when they are not
+  available now.
+
+Readings where those sections are silent:
+* the CPU pool is a FIFO free list like the GPU one (take from the front,
+  release to the back, in block-table order);
+* a swapped-out request's GPU blocks are released exactly as free_request
+  would (indexed ones become cached) and its prompt registration is
+  dropped; swap-in takes fresh, private GPU blocks in table order (evicting
+  cached blocks as reserve() would) and restores T_i;
+* swap_out and swap_in happen outside a plan (no reservation open) and stand
+  whatever later happens to the step.
 """
 
 from __future__ import annotations
@@ -100,7 +120,7 @@ class PrefixStats:
 
 class NaiveAllocator:
     def __init__(self, num_blocks: int, block_size: int, max_blocks_per_req: int | None = None,
-                 deep: bool = True):
+                 deep: bool = True, num_cpu_blocks: int = 0):
         self.deep = deep
         self.capacity = num_blocks
         self.block_size = block_size
@@ -119,6 +139,10 @@ class NaiveAllocator:
         self.prompts: dict[int, tuple] = {}      # req -> (namespace, prompt tokens)
         self.indexed_upto: dict[int, int] = {}   # req -> prompt blocks already settled
         self.pfx = PrefixStats()
+        # swapping
+        self.cpu_capacity = num_cpu_blocks
+        self.cpu_free: list[int] = list(range(num_cpu_blocks))
+        self.swapped: dict[int, tuple[list[int], int]] = {}   # req -> (CPU blocks, T_i)
         self.check()
 
     # -- queries ---------------------------------------------------------------
@@ -184,6 +208,11 @@ class NaiveAllocator:
         s = self.stats()
         if s.free + s.reserved + s.committed + s.cached != s.capacity:
             raise AllocatorError("conservation violated")
+        if len(self.cpu_free) + sum(len(c) for c, _ in self.swapped.values()) != self.cpu_capacity:
+            raise AllocatorError("CPU pool conservation violated")
+        for r, (c, t) in self.swapped.items():
+            if r in self.tables or len(c) != blocks_for(t, self.block_size):
+                raise AllocatorError("a swapped request is inconsistent")
         for r, t in self.tables.items():
             if len(t) != blocks_for(self.tokens[r], self.block_size):
                 raise AllocatorError("q_i != ceil(T_i / B)")
@@ -385,11 +414,61 @@ class NaiveAllocator:
         self.pending = None
         self.check()
 
+    # -- swapping ---------------------------------------------------------------
+    def swap_out(self, req: int):
+        """Move req's blocks to the CPU pool.  Returns ([(gpu, cpu)], released
+        GPU blocks), or None (state unchanged) if the CPU pool is too small."""
+        if self.pending is not None:
+            raise AllocatorError("swap_out while a reservation is open")
+        if req in self.swapped or not self.tables.get(req):
+            raise AllocatorError("swap_out of a request that holds no GPU blocks")
+        blocks = list(self.tables[req])
+        if len(blocks) > len(self.cpu_free):
+            return None
+        cpu = [self.cpu_free.pop(0) for _ in blocks]
+        tokens = self.tokens[req]
+        released = self._release_request(req)
+        self.swapped[req] = (cpu, tokens)
+        self.check()
+        return list(zip(blocks, cpu)), released
+
+    def swap_in_status(self, req: int) -> str:
+        n = len(self.swapped[req][0])
+        if n > self.capacity:
+            return "never"
+        return "later" if n > self.available() else "ok"
+
+    def swap_in(self, req: int) -> list[tuple[int, int]]:
+        """Bring req back into fresh GPU blocks; returns [(cpu, gpu)]."""
+        if self.pending is not None:
+            raise AllocatorError("swap_in while a reservation is open")
+        if self.swap_in_status(req) != "ok":
+            raise AllocatorError("swap_in without the blocks")
+        cpu, tokens = self.swapped.pop(req)
+        if len(self.free_list) < len(cpu):
+            self._evict(len(cpu) - len(self.free_list))
+        gpu = [self.free_list.pop(0) for _ in cpu]
+        self.tables[req] = gpu
+        self.tokens[req] = tokens
+        self.cpu_free += cpu
+        s_ = self.stats()
+        self.peak_used = max(self.peak_used, s_.reserved + s_.committed)
+        self.check()
+        return list(zip(cpu, gpu))
+
     def free_request(self, req: int) -> int:
         """Release `req`: its committed blocks in table order (each one no other
         request holds goes to the cache if indexed, else to the back of the free
-        list), then any reserved ones to the back of the free list.  Returns how
-        many blocks it held that no request holds any more."""
+        list), then any reserved ones to the back of the free list; a swapped
+        request releases its CPU blocks.  Returns how many GPU blocks it held
+        that no request holds any more."""
+        if req in self.swapped:
+            self.cpu_free += self.swapped.pop(req)[0]
+        released = self._release_request(req)
+        self.check()
+        return released
+
+    def _release_request(self, req: int) -> int:
         released = 0
         if req in self.tables:
             blocks = self.tables.pop(req)
@@ -411,5 +490,4 @@ class NaiveAllocator:
             self.pending = keep
         self.prompts.pop(req, None)
         self.indexed_upto.pop(req, None)
-        self.check()
         return released

@@ -12,6 +12,11 @@ Sources:
   with 0 <= w_i < B; and the tail-waste program over lengths [37, 81, 130, 211].
 * same page, section "分配是词元计划的一部分": the incremental demand
   delta_q_i = ceil((T_i + s_i) / B) - ceil(T_i / B).
+* same page, section "只有数据路径划算时才移动 KV 状态": a transfer of S bytes
+  over a path of measured bandwidth beta takes tau >= tau_fixed + S / beta.
+* "Chunked Prefill 与 Preemption", section "可运行等价性与成本核算": a swap's
+  payload round trip is at least 2 * cached_tokens * kv_bytes_per_token /
+  bandwidth.
 """
 
 from __future__ import annotations
@@ -94,3 +99,17 @@ def tail_waste_table(lengths, block_sizes, declared_max: int):
         allocated = entries * b
         rows.append((b, entries, allocated, allocated - sum(lengths)))
     return rows, len(lengths) * declared_max
+
+
+# -- moving KV state ------------------------------------------------------------
+def transfer_lower_bound_s(payload_bytes: int, bandwidth_bytes_per_s: float,
+                           fixed_s: float = 0.0) -> float:
+    """tau_transfer >= tau_fixed + S / beta."""
+    return fixed_s + payload_bytes / bandwidth_bytes_per_s
+
+
+def swap_roundtrip_s(cached_tokens: int, kv_bytes_per_token: int,
+                     bandwidth_bytes_per_s: float) -> float:
+    """Payload-only lower bound of swapping a request out and back in."""
+    payload = cached_tokens * kv_bytes_per_token
+    return 2 * transfer_lower_bound_s(payload, bandwidth_bytes_per_s)

@@ -53,6 +53,27 @@ recomputed request hit part of its prefix):
   evicted on demand); an admitted request's first chunk fits when its new
   blocks plus the cached blocks its match takes out of the cache fit; a
   preemption gives back the blocks no other request holds.
+
+Swap preemption ("vLLM 抢占机制源码精读", sections "Swap 模式", "CPU swap 空间
+不足时的处理" and "Swap-in 恢复流程"; "GPT-5 时代大模型推理调度系统深度实战",
+section 4.3), with preemption_mode = "swap":
+* a victim's blocks are swapped out (GPU -> CPU mapping for the transfer),
+  it keeps num_computed and goes RUNNING -> SWAPPED, to the back of the
+  swapped queue;
+* in a step without preemption the swapped queue is served head first before
+  any admission: "never" (more blocks than the pool) finishes the request as
+  ignored, "later" or a lack of budget or seats stops the loop; otherwise
+  the request is swapped in (CPU -> GPU mapping), becomes RUNNING at the back
+  of the running queue and is scheduled in this step.
+
+Readings where those sections are silent:
+* when the CPU pool cannot take a victim, the victim is preempted by
+  recompute instead (the page's engine aborts; its FIXME suggests failing
+  only the request; recompute keeps the request alive);
+* WAITING requests are admitted only once no request is left swapped, so
+  swapped requests (older) are not overtaken;
+* a swapped request's first chunk needs its swapped blocks plus the new
+  blocks of s_i = min(num_tokens - num_computed, chunk_size, budget) tokens.
 """
 
 from __future__ import annotations
@@ -63,6 +84,7 @@ from .allocator import NaiveAllocator
 from .paging import blocks_for, delta_blocks
 
 WAITING, RUNNING, FINISHED = "waiting", "running", "finished"
+SWAPPED, FINISHED_IGNORED = "swapped", "finished_ignored"
 _M64 = (1 << 64) - 1
 
 
@@ -87,6 +109,8 @@ class SchedConfig:
     artificial_preempt_prob: float = 0.0   # 0 disables the test hook
     artificial_preempt_max: int = 0
     artificial_seed: int = 0
+    preemption_mode: str = "recompute"     # or "swap"
+    num_cpu_blocks: int = 0                # the CPU pool for swapping
 
 
 @dataclass
@@ -108,22 +132,29 @@ class StepPlan:
     entries: list = field(default_factory=list)   # (rid, s, num_computed_before)
     preempted: list = field(default_factory=list)  # rids, in preemption order
     admitted: list = field(default_factory=list)   # rids admitted this step
+    swapped_out: list = field(default_factory=list)   # victims that went to the CPU pool
+    swapped_in: list = field(default_factory=list)    # rids brought back this step
+    ignored: list = field(default_factory=list)       # rids finished as ignored
+    swap_out_pairs: list = field(default_factory=list)  # (gpu block, cpu block)
+    swap_in_pairs: list = field(default_factory=list)   # (cpu block, gpu block)
 
 
 class NaiveScheduler:
     def __init__(self, cfg: SchedConfig, deep_checks: bool = True):
         self.cfg = cfg
         self.alloc = NaiveAllocator(cfg.num_blocks, cfg.block_size, cfg.max_blocks_per_req,
-                                    deep=deep_checks)
+                                    deep=deep_checks, num_cpu_blocks=cfg.num_cpu_blocks)
         self.reqs: dict[int, Request] = {}
         self.waiting: list[int] = []
         self.running: list[int] = []
+        self.swapped: list[int] = []
         self.plan: StepPlan | None = None
         self.rng_state = cfg.artificial_seed & _M64
         self.inject_left = cfg.artificial_preempt_max
         self.finished: list[int] = []
         self.total_preemptions = 0
         self.recomputed_tokens = 0
+        self.swapped_out_blocks = 0
 
     # -- requests ------------------------------------------------------------------
     def add_request(self, rid: int, prompt_len: int, max_output: int, namespace: int = 0,
@@ -149,8 +180,23 @@ class NaiveScheduler:
         return (z >> 11) * (1.0 / (1 << 53))
 
     def _preempt(self, rid: int, plan: StepPlan) -> int:
-        """Recompute preemption; returns the blocks no request holds any more."""
+        """Swap (if configured and the CPU pool has room) or recompute
+        preemption; returns the blocks no request holds any more."""
         req = self.reqs[rid]
+        if self.cfg.preemption_mode == "swap":
+            out = self.alloc.swap_out(rid)
+            if out is not None:
+                pairs, released = out
+                req.status = SWAPPED
+                req.preemptions += 1
+                self.total_preemptions += 1
+                self.swapped_out_blocks += len(pairs)
+                self.running.remove(rid)
+                self.swapped.append(rid)
+                plan.preempted.append(rid)
+                plan.swapped_out.append(rid)
+                plan.swap_out_pairs += pairs
+                return released
         self.recomputed_tokens += req.num_computed
         released = self.alloc.free_request(rid)
         req.num_computed = 0
@@ -204,8 +250,34 @@ class NaiveScheduler:
             free -= need
             i += 1
 
-        # WAITING, only in a step without preemption
+        # SWAPPED, head first, only in a step without preemption
         if not plan.preempted:
+            while self.swapped and budget > 0 and len(self.running) < c.max_num_seqs:
+                rid = self.swapped[0]
+                req = self.reqs[rid]
+                status = self.alloc.swap_in_status(rid)
+                if status == "never":
+                    self.swapped.pop(0)
+                    self.alloc.free_request(rid)
+                    req.status = FINISHED_IGNORED
+                    plan.ignored.append(rid)
+                    continue
+                cpu_blocks, tokens = self.alloc.swapped[rid]
+                s = min(req.num_tokens - req.num_computed, c.chunk_size, budget)
+                need = len(cpu_blocks) + delta_blocks(tokens, s, B)
+                if need > free:
+                    break
+                self.swapped.pop(0)
+                plan.swap_in_pairs += self.alloc.swap_in(rid)
+                req.status = RUNNING
+                self.running.append(rid)
+                plan.swapped_in.append(rid)
+                wanted.append((rid, s))
+                budget -= s
+                free -= need
+
+        # WAITING, only in a step without preemption and with nothing swapped
+        if not plan.preempted and not self.swapped:
             while self.waiting and budget > 0 and len(self.running) < c.max_num_seqs:
                 rid = self.waiting[0]
                 req = self.reqs[rid]
