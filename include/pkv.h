@@ -435,6 +435,34 @@ int pkv_alloc_cached_list(const pkv_alloc* a, int32_t* out, int32_t capacity);
 int64_t pkv_alloc_available(const pkv_alloc* a);
 
 /* ------------------------------------------------------------------------
+ * Swapping  [抢占, sections "Swap 模式" (can_swap_out, swap_out returning
+ * the GPU -> CPU block mapping, RUNNING -> SWAPPED) and "Swap-in 恢复流程"
+ * (can_swap_in: ok / later / never; swap_in returning the CPU -> GPU mapping)]
+ *
+ * The allocator keeps a pool of num_cpu_blocks host block ids, a FIFO free
+ * list like the GPU one.  swap_out(req) needs a free CPU block for each of
+ * req's GPU blocks (else PKV_E_NO_BLOCKS, nothing changes), writes the
+ * (GPU, CPU) pairs in table order, and releases the GPU blocks as
+ * free_request() would (*released = how many no request holds any more).
+ * swap_in_status: 0 ok, 1 later (not enough q_free + q_cached), 2 never
+ * (more blocks than the GPU pool).  swap_in takes fresh GPU blocks from the
+ * front of the free list (evicting cached blocks as reserve() does), writes
+ * the (CPU, GPU) pairs and releases the CPU blocks.  Neither may be called
+ * while a reservation is open.  The data itself moves with pkv_copy_blocks.
+ * ---------------------------------------------------------------------- */
+pkv_alloc* pkv_alloc_create_with_cpu_pool(int32_t num_blocks, int32_t block_size,
+                                          int32_t max_blocks_per_req, int32_t num_cpu_blocks);
+/* returns the pair count or an error */
+int pkv_alloc_swap_out(pkv_alloc* a, int32_t req_id, int32_t* pairs, int32_t capacity,
+                       int32_t* released);
+int pkv_alloc_swap_in_status(const pkv_alloc* a, int32_t req_id);
+int pkv_alloc_swap_in(pkv_alloc* a, int32_t req_id, int32_t* pairs, int32_t capacity);
+/* CPU blocks of a swapped request (0 if it is not swapped); *tokens = its T_i */
+int pkv_alloc_swapped_blocks(const pkv_alloc* a, int32_t req_id, int32_t* out, int32_t capacity,
+                             int64_t* tokens);
+int pkv_alloc_cpu_free_list(const pkv_alloc* a, int32_t* out, int32_t capacity);
+
+/* ------------------------------------------------------------------------
  * Continuous-batching scheduler (host)  [AI Infra, sections "连续批处理" and
  * "附4：vLLM调度详细流程"; 抢占, sections "抢占的触发条件", "_schedule_running 中
  * 的抢占循环", "reset_state_for_recompute 的巧妙设计", "人工抢占测试"; 显存调度,
@@ -451,8 +479,25 @@ int64_t pkv_alloc_available(const pkv_alloc* a);
  * num_computed += s_i; a request that caught up samples one token and
  * either finishes (blocks freed) or grows num_tokens by one.
  * finish_step(0) rolls the reservation back.
+ *
+ * Swap preemption (preemption_mode = PKV_PREEMPT_SWAP)  [抢占, sections
+ * "Swap 模式", "CPU swap 空间不足时的处理", "Swap-in 恢复流程"; 调度实战,
+ * section 4.3]: a victim's blocks are swapped out to a pool of
+ * num_cpu_blocks host blocks (it keeps num_computed and joins the back of
+ * the SWAPPED queue); if the CPU pool is too small it is preempted by
+ * recompute instead.  In a step without preemption the SWAPPED queue is
+ * served head first before any admission: a request with more blocks than
+ * the GPU pool finishes as ignored; one whose blocks plus its first chunk's
+ * new blocks do not fit (or with no budget or seat left) stops the loop;
+ * otherwise it is swapped in and scheduled at the back of RUNNING.  WAITING
+ * requests are admitted only when nothing is left swapped.  The step's
+ * block moves (pkv_sched_swaps) must be done with pkv_copy_blocks before
+ * the step's kernels run: first GPU -> CPU, then CPU -> GPU.
  * ---------------------------------------------------------------------- */
 typedef struct pkv_sched pkv_sched;
+
+#define PKV_PREEMPT_RECOMPUTE 0
+#define PKV_PREEMPT_SWAP 1
 
 typedef struct {
   int32_t max_num_seqs;
@@ -465,6 +510,8 @@ typedef struct {
   int32_t artificial_preempt_max;   /* test hook: at most this many forced failures */
   double artificial_preempt_prob;   /* test hook: 0 disables it */
   uint64_t artificial_seed;         /* splitmix64 seed of the test hook */
+  int32_t preemption_mode;          /* PKV_PREEMPT_RECOMPUTE (0) or PKV_PREEMPT_SWAP */
+  int32_t num_cpu_blocks;           /* host blocks for swapping (swap mode) */
 } pkv_sched_config;
 
 typedef struct {
@@ -478,7 +525,8 @@ typedef struct {
 } pkv_step_info;
 
 typedef struct {
-  int32_t status;         /* 0 waiting, 1 running, 2 finished, -1 unknown */
+  int32_t status;         /* 0 waiting, 1 running, 2 finished, 3 swapped,
+                             4 finished as ignored, -1 unknown */
   int32_t prompt_len;
   int32_t max_output;
   int32_t outputs;
@@ -506,6 +554,16 @@ int pkv_sched_step(pkv_sched* s, pkv_step_info* info);
 int pkv_sched_plan(const pkv_sched* s, int32_t* req_ids, int32_t* num_new_tokens,
                    int32_t* num_computed_before, int32_t capacity);
 int pkv_sched_preempted(const pkv_sched* s, int32_t* out, int32_t capacity);
+/* The open step's block moves: (GPU block, CPU block) pairs of its swap-outs
+ * into out_pairs[2 * out_capacity], (CPU block, GPU block) pairs of its
+ * swap-ins into in_pairs[2 * in_capacity]; *num_out / *num_in receive the
+ * counts.  Either array may be NULL with capacity 0 to query the counts. */
+int pkv_sched_swaps(const pkv_sched* s, int32_t* out_pairs, int32_t out_capacity,
+                    int32_t* num_out, int32_t* in_pairs, int32_t in_capacity, int32_t* num_in);
+/* Requests swapped out, swapped in and finished as ignored in the open step. */
+int pkv_sched_swap_events(const pkv_sched* s, int32_t* swapped_out, int32_t* num_swapped_out,
+                          int32_t* swapped_in, int32_t* num_swapped_in, int32_t* ignored,
+                          int32_t* num_ignored, int32_t capacity);
 int pkv_sched_admitted(const pkv_sched* s, int32_t* out, int32_t capacity);
 /* the open step's kernel inputs, requests in plan order: block_table rows
  * (committed + reserved blocks, unused entries -1), query_start_loc [R+1],

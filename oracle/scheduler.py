@@ -183,7 +183,7 @@ class NaiveScheduler:
         """Swap (if configured and the CPU pool has room) or recompute
         preemption; returns the blocks no request holds any more."""
         req = self.reqs[rid]
-        if self.cfg.preemption_mode == "swap":
+        if self.cfg.preemption_mode == "swap" and self.alloc.tables.get(rid):
             out = self.alloc.swap_out(rid)
             if out is not None:
                 pairs, released = out

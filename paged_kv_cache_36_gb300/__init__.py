@@ -204,11 +204,12 @@ class Allocator:
     """Reserve / commit / rollback block allocator (host)."""
 
     def __init__(self, num_blocks: int, block_size: int, max_blocks_per_req: int | None = None,
-                 _handle=None):
+                 _handle=None, num_cpu_blocks: int = 0):
         self._own = _handle is None
         self.num_blocks = num_blocks
-        self._h = _handle or lib().pkv_alloc_create(num_blocks, block_size,
-                                                    max_blocks_per_req or num_blocks)
+        self.num_cpu_blocks = num_cpu_blocks
+        self._h = _handle or lib().pkv_alloc_create_with_cpu_pool(
+            num_blocks, block_size, max_blocks_per_req or num_blocks, num_cpu_blocks)
         if not self._h:
             raise PkvError(-1, "pkv_alloc_create")
 
@@ -296,22 +297,61 @@ class Allocator:
     def available(self) -> int:
         return int(lib().pkv_alloc_available(self._h))
 
+    # -- swapping ----------------------------------------------------------------
+    def swap_out(self, req: int):
+        """([(gpu, cpu)], released) or None if the CPU pool is too small."""
+        buf = np.empty(2 * max(1, self.num_blocks), dtype=np.int32)
+        rel = C.c_int32(0)
+        n = lib().pkv_alloc_swap_out(self._h, req, _ptr(buf), len(buf) // 2, C.byref(rel))
+        if n == -4:
+            return None
+        _check(n, "swap_out")
+        return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n)], rel.value
+
+    def swap_in_status(self, req: int) -> str:
+        st = _check(lib().pkv_alloc_swap_in_status(self._h, req), "swap_in_status")
+        return ("ok", "later", "never")[st]
+
+    def swap_in(self, req: int) -> list[tuple[int, int]]:
+        buf = np.empty(2 * max(1, self.num_blocks), dtype=np.int32)
+        n = _check(lib().pkv_alloc_swap_in(self._h, req, _ptr(buf), len(buf) // 2), "swap_in")
+        return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n)]
+
+    def swapped_blocks(self, req: int):
+        """(CPU blocks, T_i) of a swapped request, or ([], 0)."""
+        buf = np.empty(max(1, self.num_cpu_blocks), dtype=np.int32)
+        tok = C.c_int64(0)
+        n = _check(lib().pkv_alloc_swapped_blocks(self._h, req, _ptr(buf), len(buf),
+                                                  C.byref(tok)), "swapped_blocks")
+        return buf[:n].tolist(), tok.value
+
+    def cpu_free_list(self) -> list[int]:
+        buf = np.empty(max(1, self.num_cpu_blocks), dtype=np.int32)
+        n = _check(lib().pkv_alloc_cpu_free_list(self._h, _ptr(buf), len(buf)), "cpu_free_list")
+        return buf[:n].tolist()
+
 
 class Scheduler:
     """Continuous-batching scheduler with recompute preemption (host)."""
 
     def __init__(self, max_num_seqs, max_num_batched_tokens, chunk_size, max_model_len,
                  block_size, num_blocks, max_blocks_per_req, artificial_preempt_prob=0.0,
-                 artificial_preempt_max=0, artificial_seed=0):
+                 artificial_preempt_max=0, artificial_seed=0, preemption_mode="recompute",
+                 num_cpu_blocks=0):
+        if preemption_mode not in ("recompute", "swap"):
+            raise ValueError("preemption_mode must be 'recompute' or 'swap'")
+        swap = preemption_mode == "swap"
         cfg = _ffi.SchedConfig(max_num_seqs, max_num_batched_tokens, chunk_size, max_model_len,
                                block_size, num_blocks, max_blocks_per_req, artificial_preempt_max,
-                               artificial_preempt_prob, artificial_seed)
+                               artificial_preempt_prob, artificial_seed, 1 if swap else 0,
+                               num_cpu_blocks)
         self._h = lib().pkv_sched_create(C.byref(cfg))
         if not self._h:
             raise PkvError(-1, "pkv_sched_create")
         self.num_blocks = num_blocks
         self.max_blocks_per_req = max_blocks_per_req
-        self.allocator = Allocator(num_blocks, block_size, _handle=lib().pkv_sched_allocator(self._h))
+        self.allocator = Allocator(num_blocks, block_size, _handle=lib().pkv_sched_allocator(self._h),
+                                   num_cpu_blocks=num_cpu_blocks if swap else 0)
         self.info = _ffi.StepInfo()
 
     def __del__(self):
@@ -345,8 +385,23 @@ class Scheduler:
         adm = np.empty(max(i.num_admitted, 1), np.int32)
         lib().pkv_sched_preempted(self._h, _ptr(pre), len(pre))
         lib().pkv_sched_admitted(self._h, _ptr(adm), len(adm))
+        no, ni = C.c_int32(0), C.c_int32(0)
+        _check(lib().pkv_sched_swaps(self._h, None, 0, C.byref(no), None, 0, C.byref(ni)), "swaps")
+        outp = np.empty(2 * max(1, no.value), np.int32)
+        inp = np.empty(2 * max(1, ni.value), np.int32)
+        _check(lib().pkv_sched_swaps(self._h, _ptr(outp), no.value, C.byref(no), _ptr(inp),
+                                     ni.value, C.byref(ni)), "swaps")
+        cap = 1 << 12
+        so, si, ig = (np.empty(cap, np.int32) for _ in range(3))
+        nso, nsi, nig = C.c_int32(0), C.c_int32(0), C.c_int32(0)
+        _check(lib().pkv_sched_swap_events(self._h, _ptr(so), C.byref(nso), _ptr(si),
+                                           C.byref(nsi), _ptr(ig), C.byref(nig), cap), "swap_events")
         return {"entries": list(zip(ids.tolist(), toks.tolist(), before.tolist())),
                 "preempted": pre[:i.num_preempted].tolist(), "admitted": adm[:i.num_admitted].tolist(),
+                "swap_out_pairs": [tuple(x) for x in outp[:2 * no.value].reshape(-1, 2).tolist()],
+                "swap_in_pairs": [tuple(x) for x in inp[:2 * ni.value].reshape(-1, 2).tolist()],
+                "swapped_out": so[:nso.value].tolist(), "swapped_in": si[:nsi.value].tolist(),
+                "ignored": ig[:nig.value].tolist(),
                 "num_tokens": int(i.num_tokens), "max_blocks": int(i.max_blocks),
                 "max_query_len": int(i.max_query_len)}
 

@@ -38,7 +38,8 @@ class SchedConfig(C.Structure):
     _fields_ = [("max_num_seqs", i32), ("max_num_batched_tokens", i32), ("chunk_size", i32),
                 ("max_model_len", i32), ("block_size", i32), ("num_blocks", i32),
                 ("max_blocks_per_req", i32), ("artificial_preempt_max", i32),
-                ("artificial_preempt_prob", f64), ("artificial_seed", u64)]
+                ("artificial_preempt_prob", f64), ("artificial_seed", u64),
+                ("preemption_mode", i32), ("num_cpu_blocks", i32)]
 
 
 class StepInfo(C.Structure):
@@ -88,6 +89,12 @@ SIGNATURES = {
     "pkv_alloc_ref_count": (C.c_int, [vp, i32]),
     "pkv_alloc_cached_list": (C.c_int, [vp, vp, i32]),
     "pkv_alloc_available": (i64, [vp]),
+    "pkv_alloc_create_with_cpu_pool": (vp, [i32, i32, i32, i32]),
+    "pkv_alloc_swap_out": (C.c_int, [vp, i32, vp, i32, vp]),
+    "pkv_alloc_swap_in_status": (C.c_int, [vp, i32]),
+    "pkv_alloc_swap_in": (C.c_int, [vp, i32, vp, i32]),
+    "pkv_alloc_swapped_blocks": (C.c_int, [vp, i32, vp, i32, vp]),
+    "pkv_alloc_cpu_free_list": (C.c_int, [vp, vp, i32]),
     "pkv_sched_create": (vp, [C.POINTER(SchedConfig)]),
     "pkv_sched_destroy": (None, [vp]),
     "pkv_sched_add_request": (C.c_int, [vp, i32, i32, i32]),
@@ -96,6 +103,8 @@ SIGNATURES = {
     "pkv_sched_plan": (C.c_int, [vp, vp, vp, vp, i32]),
     "pkv_sched_preempted": (C.c_int, [vp, vp, i32]),
     "pkv_sched_admitted": (C.c_int, [vp, vp, i32]),
+    "pkv_sched_swaps": (C.c_int, [vp, vp, i32, vp, vp, i32, vp]),
+    "pkv_sched_swap_events": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i32]),
     "pkv_sched_build_metadata": (C.c_int, [vp, vp, i32, vp, vp, vp, vp]),
     "pkv_sched_finish_step": (C.c_int, [vp, i32, vp, i32]),
     "pkv_sched_request": (C.c_int, [vp, i32, C.POINTER(RequestState)]),

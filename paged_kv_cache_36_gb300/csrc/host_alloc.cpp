@@ -30,6 +30,15 @@
 // the device copy, and commit lets go of the source; within one plan the last
 // writer of a shared block keeps the original.
 //
+// Swapping: "vLLM 抢占机制源码精读", sections "Swap 模式" and "Swap-in 恢复流程".
+// swap_out needs a free CPU block per GPU block (else nothing changes), lists
+// the GPU -> CPU pairs for the transfer and releases the GPU blocks as
+// free_request would; swap_in is "never" possible with more blocks than the
+// pool, "later" when they are not available, and otherwise takes fresh GPU
+// blocks in table order (evicting cached ones as reserve() does), lists the
+// CPU -> GPU pairs and releases the CPU blocks.  The CPU pool is a FIFO free
+// list too.
+//
 // The free list is a ring buffer over num_blocks slots, so pop-front,
 // push-back and the push-front of a rollback are O(1); the cached list is an
 // intrusive doubly linked list over block ids.  Each request keeps one vector
@@ -48,14 +57,18 @@ namespace pkv {
 
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-Allocator::Allocator(int32_t num_blocks, int32_t block_size, int32_t max_blocks_per_req)
+Allocator::Allocator(int32_t num_blocks, int32_t block_size, int32_t max_blocks_per_req,
+                     int32_t num_cpu_blocks)
     : capacity_(num_blocks), block_size_(block_size), max_blocks_per_req_(max_blocks_per_req),
       ring_(static_cast<size_t>(num_blocks)), head_(0), count_(num_blocks),
       holders_(static_cast<size_t>(num_blocks), 0), children_(static_cast<size_t>(num_blocks), 0),
       parent_(static_cast<size_t>(num_blocks), -2), key_of_(static_cast<size_t>(num_blocks)),
       lru_prev_(static_cast<size_t>(num_blocks), -1), lru_next_(static_cast<size_t>(num_blocks), -1),
-      in_cache_(static_cast<size_t>(num_blocks), 0) {
+      in_cache_(static_cast<size_t>(num_blocks), 0), cpu_capacity_(num_cpu_blocks),
+      cpu_ring_(static_cast<size_t>(num_cpu_blocks > 0 ? num_cpu_blocks : 0)),
+      cpu_count_(num_cpu_blocks > 0 ? num_cpu_blocks : 0) {
   for (int32_t i = 0; i < num_blocks; ++i) ring_[i] = i;
+  for (int32_t i = 0; i < cpu_count_; ++i) cpu_ring_[i] = i;
 }
 
 int32_t Allocator::pop_front() {
@@ -357,8 +370,21 @@ int Allocator::rollback() {
 }
 
 int Allocator::free_request(int32_t req) {
+  auto sw = swapped_.find(req);
+  if (sw != swapped_.end()) {  // a swapped request lets its CPU blocks go
+    for (int32_t c : sw->second.cpu) {
+      cpu_ring_[(cpu_head_ + cpu_count_) % cpu_capacity_] = c;
+      ++cpu_count_;
+    }
+    swapped_.erase(sw);
+  }
   auto it = reqs_.find(req);
   if (it == reqs_.end()) return 0;
+  return release_request(it);
+}
+
+int32_t Allocator::release_request(std::unordered_map<int32_t, ReqBlocks>::iterator it) {
+  const int32_t req = it->first;
   ReqBlocks& r = it->second;
   const PlanEntry* e = nullptr;
   size_t e_at = 0;
@@ -396,6 +422,86 @@ int Allocator::free_request(int32_t req) {
   }
   reqs_.erase(it);
   return released;
+}
+
+// ---------------------------------------------------------------- swapping
+int Allocator::swap_out(int32_t req, int32_t* pairs, int32_t cap_pairs, int32_t* released) {
+  if (open_) return fail(PKV_E_STATE, "swap_out: a reservation is open");
+  auto it = reqs_.find(req);
+  if (it == reqs_.end() || it->second.blocks.empty() || swapped_.count(req))
+    return fail(PKV_E_STATE, "swap_out: request %d holds no GPU blocks", req);
+  const std::vector<int32_t> blocks = it->second.blocks;
+  const int32_t n = static_cast<int32_t>(blocks.size());
+  if (n > cpu_count_)
+    return fail(PKV_E_NO_BLOCKS, "swap_out: %d blocks, %d free CPU blocks", n, cpu_count_);
+  if (n > cap_pairs || !pairs) return fail(PKV_E_INVALID, "swap_out: pair capacity %d < %d", cap_pairs, n);
+  Swapped sw;
+  sw.tokens = it->second.tokens;
+  for (int32_t k = 0; k < n; ++k) {
+    const int32_t c = cpu_ring_[cpu_head_];
+    cpu_head_ = (cpu_head_ + 1) % cpu_capacity_;
+    --cpu_count_;
+    sw.cpu.push_back(c);
+    pairs[2 * k] = blocks[k];
+    pairs[2 * k + 1] = c;
+  }
+  const int32_t rel = release_request(it);
+  if (released) *released = rel;
+  swapped_.emplace(req, std::move(sw));
+  return n;
+}
+
+int Allocator::swap_in_status(int32_t req) const {
+  auto it = swapped_.find(req);
+  if (it == swapped_.end()) return fail(PKV_E_UNKNOWN_REQ, "swap_in_status: request %d is not swapped", req);
+  const int64_t n = static_cast<int64_t>(it->second.cpu.size());
+  if (n > capacity_) return 2;
+  return n > available() ? 1 : 0;
+}
+
+int Allocator::swap_in(int32_t req, int32_t* pairs, int32_t cap_pairs) {
+  if (open_) return fail(PKV_E_STATE, "swap_in: a reservation is open");
+  const int st = swap_in_status(req);
+  if (st < 0) return st;
+  if (st != 0) return fail(PKV_E_NO_BLOCKS, "swap_in: request %d cannot be swapped in now", req);
+  auto it = swapped_.find(req);
+  const int32_t n = static_cast<int32_t>(it->second.cpu.size());
+  if (n > cap_pairs || !pairs) return fail(PKV_E_INVALID, "swap_in: pair capacity %d < %d", cap_pairs, n);
+  while (count_ < n) evict_one();
+  ReqBlocks& r = reqs_[req];
+  r = ReqBlocks();
+  for (int32_t k = 0; k < n; ++k) {
+    const int32_t g = pop_front();
+    hold(g);
+    r.blocks.push_back(g);
+    pairs[2 * k] = it->second.cpu[k];
+    pairs[2 * k + 1] = g;
+  }
+  r.committed = n;
+  r.tokens = it->second.tokens;
+  for (int32_t c : it->second.cpu) {
+    cpu_ring_[(cpu_head_ + cpu_count_) % cpu_capacity_] = c;
+    ++cpu_count_;
+  }
+  swapped_.erase(it);
+  peak_used_ = std::max<int64_t>(peak_used_, reserved_ + live_);
+  return n;
+}
+
+int Allocator::swapped_blocks(int32_t req, int32_t* out, int32_t cap, int64_t* tokens) const {
+  auto it = swapped_.find(req);
+  if (it == swapped_.end()) return 0;
+  const auto& c = it->second.cpu;
+  if (static_cast<int64_t>(c.size()) > cap) return fail(PKV_E_INVALID, "swapped_blocks: capacity");
+  if (out) std::copy(c.begin(), c.end(), out);
+  if (tokens) *tokens = it->second.tokens;
+  return static_cast<int>(c.size());
+}
+
+int Allocator::cpu_free_list(int32_t* out, int32_t cap) const {
+  if (cpu_count_ > cap) return fail(PKV_E_INVALID, "cpu_free_list: capacity %d < %d", cap, cpu_count_);
+  for (int32_t i = 0; i < cpu_count_; ++i) out[i] = cpu_ring_[(cpu_head_ + i) % cpu_capacity_];
+  return cpu_count_;
 }
 
 // ---------------------------------------------------------------- queries
@@ -556,6 +662,20 @@ int Allocator::check() const {
     indexed += parent_[b] != -2;
   }
   if (indexed != static_cast<int64_t>(index_.size())) return fail(PKV_E_STATE, "index size");
+  std::vector<uint8_t> cpu_seen(static_cast<size_t>(cpu_capacity_ > 0 ? cpu_capacity_ : 0), 0);
+  for (int32_t i = 0; i < cpu_count_; ++i) {
+    const int32_t c = cpu_ring_[(cpu_head_ + i) % cpu_capacity_];
+    if (c < 0 || c >= cpu_capacity_ || cpu_seen[c]++) return fail(PKV_E_STATE, "CPU free list corrupt");
+  }
+  for (const auto& kv : swapped_) {
+    if (reqs_.count(kv.first)) return fail(PKV_E_STATE, "request %d swapped and resident", kv.first);
+    if (static_cast<int64_t>(kv.second.cpu.size()) != ceil_div(kv.second.tokens, block_size_))
+      return fail(PKV_E_STATE, "swapped request %d: q_i != ceil(T_i/B)", kv.first);
+    for (int32_t c : kv.second.cpu)
+      if (c < 0 || c >= cpu_capacity_ || cpu_seen[c]++) return fail(PKV_E_STATE, "CPU block %d twice", c);
+  }
+  for (int32_t c = 0; c < cpu_capacity_; ++c)
+    if (!cpu_seen[c]) return fail(PKV_E_STATE, "CPU block %d is lost", c);
   return ok();
 }
 
@@ -655,5 +775,41 @@ int pkv_alloc_cached_list(const pkv_alloc* a, int32_t* out, int32_t capacity) {
   return a->impl.cached_list(out, capacity);
 }
 int64_t pkv_alloc_available(const pkv_alloc* a) { return a ? a->impl.available() : 0; }
+
+pkv_alloc* pkv_alloc_create_with_cpu_pool(int32_t num_blocks, int32_t block_size,
+                                          int32_t max_blocks_per_req, int32_t num_cpu_blocks) {
+  if (num_blocks <= 0 || block_size <= 0 || max_blocks_per_req <= 0 || num_cpu_blocks < 0) {
+    fail(PKV_E_INVALID, "pkv_alloc_create_with_cpu_pool: bad sizes");
+    return nullptr;
+  }
+  try {
+    return new pkv_alloc(num_blocks, block_size, max_blocks_per_req, num_cpu_blocks);
+  } catch (...) {
+    fail(PKV_E_INVALID, "pkv_alloc_create_with_cpu_pool: out of host memory");
+    return nullptr;
+  }
+}
+int pkv_alloc_swap_out(pkv_alloc* a, int32_t req, int32_t* pairs, int32_t capacity,
+                       int32_t* released) {
+  PKV_NEED(a);
+  return a->impl.swap_out(req, pairs, capacity, released);
+}
+int pkv_alloc_swap_in_status(const pkv_alloc* a, int32_t req) {
+  PKV_NEED(a);
+  return a->impl.swap_in_status(req);
+}
+int pkv_alloc_swap_in(pkv_alloc* a, int32_t req, int32_t* pairs, int32_t capacity) {
+  PKV_NEED(a);
+  return a->impl.swap_in(req, pairs, capacity);
+}
+int pkv_alloc_swapped_blocks(const pkv_alloc* a, int32_t req, int32_t* out, int32_t capacity,
+                             int64_t* tokens) {
+  PKV_NEED(a);
+  return a->impl.swapped_blocks(req, out, capacity, tokens);
+}
+int pkv_alloc_cpu_free_list(const pkv_alloc* a, int32_t* out, int32_t capacity) {
+  PKV_NEED(a);
+  return a->impl.cpu_free_list(out, capacity);
+}
 
 }  // extern "C"

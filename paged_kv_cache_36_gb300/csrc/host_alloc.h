@@ -12,7 +12,8 @@ namespace pkv {
 
 class Allocator {
  public:
-  Allocator(int32_t num_blocks, int32_t block_size, int32_t max_blocks_per_req);
+  Allocator(int32_t num_blocks, int32_t block_size, int32_t max_blocks_per_req,
+            int32_t num_cpu_blocks = 0);
 
   int reserve(int32_t n, const int32_t* ids, const int32_t* new_tokens);
   int commit();
@@ -43,6 +44,16 @@ class Allocator {
   // `copied_away` carries the plan's earlier copies of shared partial blocks
   int64_t plan_need(int32_t req, int32_t s, std::unordered_map<int32_t, int32_t>* copied_away) const;
 
+  // swapping: swap_out returns the pair count (GPU, CPU) written to `pairs`
+  // or PKV_E_NO_BLOCKS when the CPU pool is too small (state unchanged);
+  // swap_in_status is 0 (ok), 1 (later) or 2 (never); swap_in returns the
+  // pair count (CPU, GPU)
+  int swap_out(int32_t req, int32_t* pairs, int32_t cap_pairs, int32_t* released);
+  int swap_in_status(int32_t req) const;
+  int swap_in(int32_t req, int32_t* pairs, int32_t cap_pairs);
+  int swapped_blocks(int32_t req, int32_t* out, int32_t cap, int64_t* tokens) const;
+  int cpu_free_list(int32_t* out, int32_t cap) const;
+  int32_t cpu_free() const { return cpu_count_; }
  private:
   struct ReqBlocks {
     // committed blocks (a copy-on-write destination stands in for its source
@@ -67,6 +78,11 @@ class Allocator {
   int32_t pop_front();
   void push_back(int32_t b);
   void push_front(int32_t b);
+  int32_t release_request(std::unordered_map<int32_t, ReqBlocks>::iterator it);
+  struct Swapped {
+    std::vector<int32_t> cpu;
+    int64_t tokens;
+  };
   void hold(int32_t b);
   void unhold(int32_t b);           // a request lets go; releases the block at 0
   void release(int32_t b);          // held by no request: cached if indexed, else free
@@ -97,6 +113,11 @@ class Allocator {
   // prefix index: key (namespace, parent, block_size tokens) -> block
   std::unordered_map<std::string, int32_t> index_;
   int64_t lookups_ = 0, hits_ = 0, matched_tokens_ = 0, evictions_ = 0, cow_copies_ = 0;
+  // CPU pool for swapping: a FIFO free list (front to take, back to release)
+  int32_t cpu_capacity_;
+  std::vector<int32_t> cpu_ring_;
+  int32_t cpu_head_ = 0, cpu_count_ = 0;
+  std::unordered_map<int32_t, Swapped> swapped_;
 };
 
 }  // namespace pkv
@@ -104,5 +125,5 @@ class Allocator {
 // The opaque handle of the C interface wraps exactly one allocator.
 struct pkv_alloc {
   pkv::Allocator impl;
-  pkv_alloc(int32_t nb, int32_t bs, int32_t mb) : impl(nb, bs, mb) {}
+  pkv_alloc(int32_t nb, int32_t bs, int32_t mb, int32_t ncpu = 0) : impl(nb, bs, mb, ncpu) {}
 };

@@ -56,7 +56,7 @@ struct SplitMix64 {
   double uniform() { return static_cast<double>(next() >> 11) * (1.0 / 9007199254740992.0); }
 };
 
-enum Status : int32_t { kWaiting = 0, kRunning = 1, kFinished = 2 };
+enum Status : int32_t { kWaiting = 0, kRunning = 1, kFinished = 2, kSwapped = 3, kIgnored = 4 };
 
 struct Req {
   int32_t id;
@@ -81,7 +81,10 @@ struct Entry {
 class Scheduler {
  public:
   explicit Scheduler(const pkv_sched_config& c)
-      : cfg_(c), handle_(c.num_blocks, c.block_size, c.max_blocks_per_req), alloc_(handle_.impl),
+      : cfg_(c),
+        handle_(c.num_blocks, c.block_size, c.max_blocks_per_req,
+                c.preemption_mode == PKV_PREEMPT_SWAP ? c.num_cpu_blocks : 0),
+        alloc_(handle_.impl),
         rng_{c.artificial_seed}, inject_left_(c.artificial_preempt_max) {}
 
   int add_request(int32_t id, int32_t prompt, int32_t max_output, uint64_t ns = 0,
@@ -110,6 +113,11 @@ class Scheduler {
     entries_.clear();
     preempted_.clear();
     admitted_.clear();
+    swapped_out_.clear();
+    swapped_in_.clear();
+    ignored_.clear();
+    swap_out_pairs_.clear();
+    swap_in_pairs_.clear();
     const int32_t B = cfg_.block_size;
     int64_t budget = cfg_.max_num_batched_tokens;
     int64_t free_blocks = alloc_.available();
@@ -149,8 +157,43 @@ class Scheduler {
       ++i;
     }
 
-    // WAITING admission, only when nothing was preempted in this step.
+    // SWAPPED, head first, only when nothing was preempted in this step.
     if (preempted_.empty()) {
+      while (!swapped_.empty() && budget > 0 &&
+             static_cast<int64_t>(running_.size()) < cfg_.max_num_seqs) {
+        Req& r = reqs_.at(swapped_.front());
+        const int st = alloc_.swap_in_status(r.id);
+        if (st < 0) return st;
+        if (st == 2) {  // never: more blocks than the pool
+          swapped_.pop_front();
+          alloc_.free_request(r.id);
+          r.status = kIgnored;
+          ignored_.push_back(r.id);
+          continue;
+        }
+        int64_t tokens = 0;
+        const int n = alloc_.swapped_blocks(r.id, nullptr, 0x7fffffff, &tokens);
+        if (n < 0) return n;
+        const int64_t s = std::min<int64_t>({r.num_tokens - r.num_computed, cfg_.chunk_size, budget});
+        const int64_t need = n + ceil_div64(tokens + s, B) - ceil_div64(tokens, B);
+        if (need > free_blocks) break;
+        swapped_.pop_front();
+        std::vector<int32_t> pairs(2 * static_cast<size_t>(n));
+        const int got = alloc_.swap_in(r.id, pairs.data(), n);
+        if (got < 0) return got;
+        swap_in_pairs_.insert(swap_in_pairs_.end(), pairs.begin(), pairs.end());
+        r.status = kRunning;
+        running_.push_back(r.id);
+        swapped_in_.push_back(r.id);
+        entries_.push_back({r.id, static_cast<int32_t>(s), r.num_computed});
+        budget -= s;
+        free_blocks -= need;
+      }
+    }
+
+    // WAITING admission, only when nothing was preempted in this step and
+    // nothing is left swapped.
+    if (preempted_.empty() && swapped_.empty()) {
       while (!waiting_.empty() && budget > 0 &&
              static_cast<int64_t>(running_.size()) < cfg_.max_num_seqs) {
         Req& r = reqs_.at(waiting_.front());
@@ -251,6 +294,12 @@ class Scheduler {
   const std::vector<Entry>& entries() const { return entries_; }
   const std::vector<int32_t>& preempted() const { return preempted_; }
   const std::vector<int32_t>& admitted() const { return admitted_; }
+  const std::vector<int32_t>& swapped_out() const { return swapped_out_; }
+  const std::vector<int32_t>& swapped_in() const { return swapped_in_; }
+  const std::vector<int32_t>& ignored() const { return ignored_; }
+  const std::vector<int32_t>& swap_out_pairs() const { return swap_out_pairs_; }
+  const std::vector<int32_t>& swap_in_pairs() const { return swap_in_pairs_; }
+  const std::deque<int32_t>& swapped_queue() const { return swapped_; }
   const std::vector<int32_t>& running() const { return running_; }
   const std::deque<int32_t>& waiting() const { return waiting_; }
   const pkv_alloc* handle() const { return &handle_; }
@@ -264,11 +313,34 @@ class Scheduler {
     out[2] = finished_count_;
     out[3] = inject_left_;
   }
+  int64_t swapped_out_blocks() const { return swapped_out_blocks_; }
 
  private:
-  // Recompute preemption: returns how many blocks the request gave back.
+  // Swap (if configured and the CPU pool has room) or recompute preemption:
+  // returns how many blocks no request holds any more.
   int64_t preempt(int32_t id) {
     Req& r = reqs_.at(id);
+    if (cfg_.preemption_mode == PKV_PREEMPT_SWAP) {
+      const std::vector<int32_t>* row = alloc_.blocks(id);
+      const int32_t n = row ? static_cast<int32_t>(row->size()) : 0;
+      if (n > 0 && n <= alloc_.cpu_free()) {
+        std::vector<int32_t> pairs(2 * static_cast<size_t>(n));
+        int32_t released = 0;
+        const int got = alloc_.swap_out(id, pairs.data(), n, &released);
+        if (got == n) {
+          swap_out_pairs_.insert(swap_out_pairs_.end(), pairs.begin(), pairs.end());
+          swapped_out_blocks_ += n;
+          r.status = kSwapped;
+          ++r.preemptions;
+          ++total_preemptions_;
+          running_.erase(std::find(running_.begin(), running_.end(), id));
+          swapped_.push_back(id);
+          preempted_.push_back(id);
+          swapped_out_.push_back(id);
+          return released;
+        }
+      }
+    }
     recomputed_tokens_ += r.num_computed;
     const int released = alloc_.free_request(id);
     r.num_computed = 0;
@@ -305,8 +377,11 @@ class Scheduler {
   std::deque<int32_t> waiting_;
   std::vector<Entry> entries_;
   std::vector<int32_t> preempted_, admitted_;
+  std::deque<int32_t> swapped_;
+  std::vector<int32_t> swapped_out_, swapped_in_, ignored_, swap_out_pairs_, swap_in_pairs_;
   bool open_ = false;
   int64_t total_preemptions_ = 0, recomputed_tokens_ = 0, finished_count_ = 0;
+  int64_t swapped_out_blocks_ = 0;
 };
 
 }  // namespace pkv
@@ -324,7 +399,9 @@ pkv_sched* pkv_sched_create(const pkv_sched_config* c) {
   if (!c || c->max_num_seqs <= 0 || c->max_num_batched_tokens <= 0 || c->chunk_size <= 0 ||
       c->max_model_len <= 1 || c->block_size <= 0 || c->num_blocks <= 0 ||
       c->max_blocks_per_req <= 0 || c->artificial_preempt_prob < 0.0 ||
-      c->artificial_preempt_max < 0) {
+      c->artificial_preempt_max < 0 ||
+      (c->preemption_mode != PKV_PREEMPT_RECOMPUTE && c->preemption_mode != PKV_PREEMPT_SWAP) ||
+      c->num_cpu_blocks < 0) {
     fail(PKV_E_INVALID, "pkv_sched_create: invalid configuration");
     return nullptr;
   }
@@ -384,6 +461,40 @@ int pkv_sched_preempted(const pkv_sched* s, int32_t* out, int32_t cap) {
 int pkv_sched_admitted(const pkv_sched* s, int32_t* out, int32_t cap) {
   PKV_NEED_S(s);
   return copy_ids(s->impl.admitted(), out, cap);
+}
+
+int pkv_sched_swaps(const pkv_sched* s, int32_t* out_pairs, int32_t out_cap, int32_t* num_out,
+                    int32_t* in_pairs, int32_t in_cap, int32_t* num_in) {
+  PKV_NEED_S(s);
+  const auto& o = s->impl.swap_out_pairs();
+  const auto& i = s->impl.swap_in_pairs();
+  const int32_t no = static_cast<int32_t>(o.size() / 2), ni = static_cast<int32_t>(i.size() / 2);
+  if (num_out) *num_out = no;
+  if (num_in) *num_in = ni;
+  if (out_pairs) {
+    if (no > out_cap) return fail(PKV_E_INVALID, "pkv_sched_swaps: capacity %d < %d", out_cap, no);
+    std::copy(o.begin(), o.end(), out_pairs);
+  }
+  if (in_pairs) {
+    if (ni > in_cap) return fail(PKV_E_INVALID, "pkv_sched_swaps: capacity %d < %d", in_cap, ni);
+    std::copy(i.begin(), i.end(), in_pairs);
+  }
+  return PKV_OK;
+}
+
+int pkv_sched_swap_events(const pkv_sched* s, int32_t* so, int32_t* nso, int32_t* si, int32_t* nsi,
+                          int32_t* ig, int32_t* nig, int32_t cap) {
+  PKV_NEED_S(s);
+  const int a = copy_ids(s->impl.swapped_out(), so, cap);
+  if (a < 0) return a;
+  const int b = copy_ids(s->impl.swapped_in(), si, cap);
+  if (b < 0) return b;
+  const int c = copy_ids(s->impl.ignored(), ig, cap);
+  if (c < 0) return c;
+  if (nso) *nso = a;
+  if (nsi) *nsi = b;
+  if (nig) *nig = c;
+  return PKV_OK;
 }
 
 int pkv_sched_build_metadata(const pkv_sched* s, int32_t* bt, int32_t stride, int32_t* qsl,

@@ -94,7 +94,8 @@ def _pair(c: SchedConfig):
     ref = NaiveScheduler(c, deep_checks=False)
     cpp = pkv.Scheduler(c.max_num_seqs, c.max_num_batched_tokens, c.chunk_size, c.max_model_len,
                         c.block_size, c.num_blocks, c.max_blocks_per_req,
-                        c.artificial_preempt_prob, c.artificial_preempt_max, c.artificial_seed)
+                        c.artificial_preempt_prob, c.artificial_preempt_max, c.artificial_seed,
+                        c.preemption_mode, c.num_cpu_blocks)
     return cpp, ref
 
 
@@ -111,6 +112,9 @@ def _compare_step(cpp, ref, arrivals_now, fail_step=False, check_tables=True):
     assert pc["entries"] == pr.entries
     assert pc["preempted"] == pr.preempted
     assert pc["admitted"] == pr.admitted
+    assert pc["swapped_out"] == pr.swapped_out and pc["swapped_in"] == pr.swapped_in
+    assert pc["ignored"] == pr.ignored
+    assert pc["swap_out_pairs"] == pr.swap_out_pairs and pc["swap_in_pairs"] == pr.swap_in_pairs
     bt, qsl, seq, nc, slots = cpp.metadata()
     rqsl, rseq, rnc, rrows, rslots = ref.metadata(pr)
     assert qsl.tolist() == rqsl and seq.tolist() == rseq and nc.tolist() == rnc
@@ -267,3 +271,102 @@ def test_scheduler_prefix_trace_bit_exact():
     cnt = cpp.counters()
     assert cnt["preemptions"] == ref.total_preemptions
     assert cnt["recomputed_tokens"] == ref.recomputed_tokens
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_scheduler_swap_mode_small_random_with_faults(seed):
+    rng = random.Random(50 + seed)
+    c = SchedConfig(max_num_seqs=rng.choice([2, 4, 8]), max_num_batched_tokens=rng.choice([8, 20, 64]),
+                    chunk_size=rng.choice([3, 8, 16]), max_model_len=200, block_size=4,
+                    num_blocks=rng.choice([12, 24]), max_blocks_per_req=50,
+                    artificial_preempt_prob=0.3, artificial_preempt_max=rng.choice([0, 20]),
+                    artificial_seed=seed, preemption_mode="swap",
+                    num_cpu_blocks=rng.choice([4, 16, 200]))
+    cpp, ref = _pair(c)
+    rid = 0
+    swaps = 0
+    for step in range(250):
+        arrivals = []
+        for _ in range(rng.choice([0, 0, 1, 2])):
+            arrivals.append(type("A", (), {"req_id": rid, "prompt_len": rng.randint(1, 30),
+                                           "max_output": rng.randint(1, 12)})())
+            rid += 1
+        pc = _compare_step(cpp, ref, arrivals, fail_step=rng.random() < 0.1)
+        swaps += len(pc["swapped_out"])
+        cpp.allocator.check()
+        assert cpp.allocator.cpu_free_list() == ref.alloc.cpu_free
+    assert swaps > 0
+    assert cpp.counters()["recomputed_tokens"] == ref.recomputed_tokens
+
+
+def test_scheduler_trace_swap_mode_bit_exact():
+    """The 300-step trace with swap preemption and a 4096-block CPU pool."""
+    spec = trace_spec()
+    c = SchedConfig(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                    spec.max_model_len, spec.block_size, spec.num_blocks,
+                    spec.max_model_len // spec.block_size, preemption_mode="swap",
+                    num_cpu_blocks=4096)
+    cpp, ref = _pair(c)
+    by_step = {}
+    for a in generate_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    swaps = swapins = 0
+    for step in range(spec.steps):
+        pc = _compare_step(cpp, ref, by_step.get(step, []), check_tables=(step % 10 == 0))
+        swaps += len(pc["swapped_out"])
+        swapins += len(pc["swapped_in"])
+        if step % 25 == 0:
+            cpp.allocator.check()
+            assert cpp.allocator.cpu_free_list() == ref.alloc.cpu_free
+    assert swaps > 10 and swapins > 10
+    cnt = cpp.counters()
+    assert cnt["preemptions"] == ref.total_preemptions
+    assert cnt["recomputed_tokens"] == ref.recomputed_tokens
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_allocator_swap_random_ops(seed):
+    rng = random.Random(200 + seed)
+    B = rng.choice([2, 4])
+    nb, ncpu = rng.choice([16, 40]), rng.choice([6, 30])
+    cpp = pkv.Allocator(nb, B, 64, num_cpu_blocks=ncpu)
+    ref = NaiveAllocator(nb, B, 64, num_cpu_blocks=ncpu)
+    bases = [[rng.randrange(3) for _ in range(5 * B)] for _ in range(2)]
+    live, swapped, ids = [], [], []
+    nxt = 0
+    for _ in range(400):
+        op = rng.random()
+        if op < 0.2 and len(live) < 8:
+            toks = rng.choice(bases)[:rng.randint(1, 5 * B)]
+            assert cpp.match_prefix(nxt, 0, toks) == ref.match_prefix(nxt, 0, toks)
+            live.append(nxt); ids.append(nxt); nxt += 1
+        elif op < 0.55 and live:
+            plan = [(r, rng.randint(0, 2 * B)) for r in rng.sample(live, rng.randint(1, min(3, len(live))))]
+            a, b = cpp.reserve(plan), ref.reserve(plan)
+            assert a == b
+            if a:
+                if rng.random() < 0.8:
+                    cpp.commit(); ref.commit()
+                else:
+                    cpp.rollback(); ref.rollback()
+        elif op < 0.7 and live:
+            r = rng.choice(live)
+            if ref.tables.get(r):
+                a, b = cpp.swap_out(r), ref.swap_out(r)
+                assert a == b
+                if a is not None:
+                    live.remove(r); swapped.append(r)
+        elif op < 0.85 and swapped:
+            r = rng.choice(swapped)
+            st = ref.swap_in_status(r)
+            assert cpp.swap_in_status(r) == st
+            assert cpp.swapped_blocks(r) == (ref.swapped[r][0], ref.swapped[r][1])
+            if st == "ok":
+                assert cpp.swap_in(r) == ref.swap_in(r)
+                swapped.remove(r); live.append(r)
+        elif live or swapped:
+            r = rng.choice(live + swapped)
+            assert cpp.free_request(r) == ref.free_request(r)
+            (live if r in live else swapped).remove(r)
+        _same_prefix_alloc(cpp, ref, ids)
+        assert cpp.cpu_free_list() == ref.cpu_free
