@@ -507,6 +507,84 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     res["copy_blocks"] = res_copy
     del kc, vc, hk, hv
     torch.cuda.empty_cache()
+    # ---- the base trace with swap preemption (block moves in the timed step) ----
+    spec = trace_spec()
+    H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    ncpu = 4096
+    sched = pkv.Scheduler(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                          spec.max_model_len, B, spec.num_blocks, spec.max_model_len // B,
+                          preemption_mode="swap", num_cpu_blocks=ncpu)
+    kc = torch.zeros((spec.num_blocks, B, Hkv, D), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    hk = torch.zeros((ncpu, B, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    ws = pkv.new_workspace(spec.max_num_seqs, H, D, device)
+    budget = spec.max_num_batched_tokens
+    qp = torch.randn((budget, H, D), generator=g, device=device).to(torch.bfloat16)
+    kp = torch.randn((budget, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    vp = torch.randn((budget, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    by_step = {}
+    for a in generate_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    toks_done, ms_total, moved_blocks, ms_moves = 0, 0.0, 0, 0.0
+    for st in range(spec.steps):
+        for a in by_step.get(st, []):
+            sched.add_request(a.req_id, a.prompt_len, a.max_output)
+        plan = sched.step()
+        bt, qsl, seq, nc, slots = sched.metadata()
+        T = int(qsl[-1])
+        dev = [torch.from_numpy(x).to(device) for x in (bt, qsl, seq, nc, slots)]
+        outp = torch.tensor(plan["swap_out_pairs"], dtype=torch.int32).reshape(-1, 2).to(device)
+        inp = torch.tensor(plan["swap_in_pairs"], dtype=torch.int32).reshape(-1, 2).to(device)
+        a_ev, m_ev, b_ev = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a_ev.record(stream)
+        if outp.shape[0]:
+            pkv.copy_blocks(kc, vc, hk, hv, outp)
+        if inp.shape[0]:
+            pkv.copy_blocks(hk, hv, kc, vc, inp)
+        m_ev.record(stream)
+        if T:
+            pkv.reshape_and_cache(kp[:T], vp[:T], kc, vc, dev[4])
+            pkv.paged_attention_varlen(qp[:T], kc, vc, dev[0], dev[1], dev[2], dev[3],
+                                       1.0 / math.sqrt(D), workspace=ws,
+                                       max_query_len=plan["max_query_len"])
+        b_ev.record(stream)
+        b_ev.synchronize()
+        toks_done += T
+        ms_total += a_ev.elapsed_time(b_ev)
+        ms_moves += a_ev.elapsed_time(m_ev)
+        moved_blocks += outp.shape[0] + inp.shape[0]
+        sched.finish_step(True)
+    cnt = sched.counters()
+    block_bytes = 2 * B * Hkv * D * 2
+    res["trace_swap"] = {
+        "workload": "the 300-step trace above with swap preemption and a 4096-block pinned "
+                    "host pool; swap-outs then swap-ins run with copy_blocks inside each "
+                    "step's timed region",
+        "tokens": toks_done, "tokens_per_s_per_layer": toks_done / (ms_total * 1e-3),
+        "preemptions": int(cnt["preemptions"]), "recomputed_tokens": int(cnt["recomputed_tokens"]),
+        "blocks_moved": int(moved_blocks), "ms_moving_blocks": ms_moves,
+        "moved_gbs": moved_blocks * block_bytes / max(ms_moves * 1e-3, 1e-9) / 1e9,
+    }
+    # the swap round trip of one 4096-token request against the page's bound
+    nreq = 256                                           # blocks of 16 tokens
+    blk = torch.arange(nreq, dtype=torch.int32, device=device)
+    pairs = torch.stack([blk, blk], 1).contiguous()
+    for _ in range(3):
+        pkv.copy_blocks(kc, vc, hk, hv, pairs)
+        pkv.copy_blocks(hk, hv, kc, vc, pairs)
+    rt = event_time(lambda: (pkv.copy_blocks(kc, vc, hk, hv, pairs),
+                             pkv.copy_blocks(hk, hv, kc, vc, pairs)), 20, stream)
+    one_way = event_time(lambda: pkv.copy_blocks(kc, vc, hk, hv, pairs), 20, stream)
+    payload = nreq * block_bytes
+    res["swap_roundtrip_4096_tokens"] = {
+        "payload_bytes": payload, "measured_ms": rt,
+        "bound_ms_from_one_way_bandwidth": 2 * payload / (payload / (one_way * 1e-3)) * 1e3,
+        "note": "bound = 2 * payload / beta (page: Chunked Prefill 与 Preemption), beta = the "
+                "measured one-way copy rate of the same blocks",
+    }
+    del kc, vc, hk, hv, ws, sched
+    torch.cuda.empty_cache()
     # ---- the trace with shared system prompts (prefix sharing on) ----
     from workloads import generate_prefix_arrivals
     spec = trace_spec()

@@ -149,10 +149,9 @@ def test_rope_rows_too_large_for_the_ring(is_neox):
 
 
 def test_rope_many_tokens_per_cta():
-    """160000 tokens of 8 + 2 heads: each CTA of the staged form takes about
-    70 consecutive tokens, so it reloads its positions past the first 32 and
-    wraps its 4-stage ring many times.  V rows and untouched slots are checked
-    bit for bit, Q and K of 2048 sampled tokens against the oracle."""
+    """160000 tokens of 8 + 2 heads (the one-warp-per-token form, each warp
+    looping over many tokens).  V rows and untouched slots are checked bit
+    for bit, Q and K of 2048 sampled tokens against the oracle."""
     T, H, Hkv, D, NB, B = 160000, 8, 2, 128, 10240, 16
     _large_case_check("ropemany", T, H, Hkv, D, NB, B,
                       uniform_int(0, 4095, T, "ropemany", "pos"), 4096,

@@ -188,3 +188,97 @@ def test_prefix_sharing_trace_300_steps():
     assert pkv.read_error_word(ws) == 0
     st = cpp.allocator.prefix_stats()
     assert st["hits"] > 100 and matched_reqs > 50 and checked >= spec.steps // CHECK_EVERY - 1
+
+
+def test_swap_preemption_trace_300_steps():
+    """The trace with swap preemption: a 2048-block pool in pinned host
+    memory receives the victims' blocks (copy_blocks, GPU -> host) and gives
+    them back on swap-in (host -> GPU) before the step's kernels; swapped
+    requests resume from their restored cache without recomputation, and
+    attention over their histories is checked against the oracle."""
+    import paged_kv_cache_36_gb300 as pkv
+    spec = trace_spec()
+    H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    mbpr = spec.max_model_len // B
+    ncpu = 2048
+    c = SchedConfig(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
+                    spec.max_model_len, B, spec.num_blocks, mbpr, preemption_mode="swap",
+                    num_cpu_blocks=ncpu)
+    ref = NaiveScheduler(c, deep_checks=False)
+    cpp = pkv.Scheduler(c.max_num_seqs, c.max_num_batched_tokens, c.chunk_size, c.max_model_len,
+                        B, c.num_blocks, mbpr, preemption_mode="swap", num_cpu_blocks=ncpu)
+    kv_rows = PooledRows(Hkv * D, "swap_kv")
+    q_rows = PooledRows(H * D, "swap_q")
+    kc = torch.zeros(spec.num_blocks, B, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    hk = torch.zeros((ncpu, B, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    ws = pkv.new_workspace(spec.max_num_seqs, H, D)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hist = {}
+    by_step = {}
+    for a in generate_arrivals(spec):
+        by_step.setdefault(a.step, []).append(a)
+    checked = swaps_out = swaps_in = resumed_checked = 0
+    for step in range(spec.steps):
+        for a in by_step.get(step, []):
+            assert cpp.add_request(a.req_id, a.prompt_len, a.max_output) == \
+                ref.add_request(a.req_id, a.prompt_len, a.max_output)
+        pc, pr = cpp.step(), ref.step()
+        assert pc["entries"] == pr.entries and pc["preempted"] == pr.preempted
+        assert pc["swap_out_pairs"] == pr.swap_out_pairs
+        assert pc["swap_in_pairs"] == pr.swap_in_pairs
+        for rid in pr.preempted:
+            if rid not in pr.swapped_out:
+                hist.pop(rid, None)            # recompute fallback: history restarts
+        if pr.swap_out_pairs:
+            pkv.copy_blocks(kc, vc, hk, hv, torch.tensor(pr.swap_out_pairs, dtype=torch.int32,
+                                                         device="cuda"), error_word=err)
+            swaps_out += len(pr.swapped_out)
+        if pr.swap_in_pairs:
+            pkv.copy_blocks(hk, hv, kc, vc, torch.tensor(pr.swap_in_pairs, dtype=torch.int32,
+                                                         device="cuda"), error_word=err)
+            swaps_in += len(pr.swapped_in)
+        bt, qsl, seq, nc, slots = cpp.metadata()
+        rqsl, rseq, rnc, rrows, rslots = ref.metadata(pr)
+        assert qsl.tolist() == rqsl and seq.tolist() == rseq and nc.tolist() == rnc
+        assert slots.tolist() == rslots
+        T = int(qsl[-1])
+        if T:
+            rid_of = np.repeat([e[0] for e in pr.entries], [e[1] for e in pr.entries])
+            pos = np.concatenate([np.arange(e[2], e[2] + e[1]) for e in pr.entries])
+            kn = kv_rows.rows(0, rid_of, pos).view(T, Hkv, D)
+            vn = kv_rows.rows(1, rid_of, pos).view(T, Hkv, D)
+            q = q_rows.rows(2, np.full(T, step), np.arange(T)).view(T, H, D)
+            at = 0
+            for rid, s, ncb in pr.entries:
+                if ncb == 0:
+                    hist[rid] = (kn[at:at + s].clone(), vn[at:at + s].clone())
+                else:
+                    k0, v0 = hist[rid]
+                    assert k0.shape[0] == ncb
+                    hist[rid] = (torch.cat([k0, kn[at:at + s]]), torch.cat([v0, vn[at:at + s]]))
+                at += s
+            pkv.reshape_and_cache(kn.cuda(), vn.cuda(), kc, vc, torch.from_numpy(slots).cuda())
+            out = pkv.paged_attention_varlen(
+                q.cuda(), kc, vc, torch.from_numpy(bt).cuda(), torch.from_numpy(qsl).cuda(),
+                torch.from_numpy(seq).cuda(), torch.from_numpy(nc).cuda(), 1.0 / math.sqrt(D),
+                workspace=ws, max_query_len=pc["max_query_len"])
+            if step % CHECK_EVERY == 0 or pr.swapped_in:
+                rows = None
+                if step % CHECK_EVERY != 0:   # just the requests restored in this step
+                    rows = [k for k, e in enumerate(pr.entries) if e[0] in pr.swapped_in]
+                    resumed_checked += len(rows)
+                histories = [hist[rid] for rid, _, _ in pr.entries]
+                want = oa.paged_attention_varlen(q, histories, qsl, seq, nc, 1.0 / math.sqrt(D),
+                                                 rows=rows)
+                compare(out, want, qsl, torch.bfloat16, rows=rows)
+                assert pkv.read_error_word(ws) == 0
+                checked += 1
+        fin_c, fin_r = cpp.finish_step(True), ref.finish_step(True)
+        assert fin_c == fin_r
+        for rid in fin_r:
+            hist.pop(rid, None)
+    torch.cuda.synchronize()
+    assert pkv.read_error_word(ws) == 0 and err.item() == 0
+    assert swaps_out > 10 and swaps_in > 10 and resumed_checked > 10
