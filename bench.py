@@ -421,7 +421,13 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         pkv.reshape_and_cache(kn, vn, kc, vc, slots)
     for _ in range(8):
         k1()
-    ms = event_time(k1, 40, stream)
+    ms_eager = event_time(k1, 40, stream)
+
+    def k1_b(b):
+        kn, vn, slots = batches[b]
+        pkv.reshape_and_cache(kn, vn, kc, vc, slots)
+    # graph-timed: an eager call's host work is close to the kernel's time
+    ms = graph_time([functools.partial(k1_b, c % 4) for c in range(40)])
     k1_bytes = T * (2 * Hkv * D * 2) * 2 + 8 * T
     res["reshape_and_cache_8192"] = {
         "workload": "8192 new tokens, 8 KV heads x 128 dims bf16, whole 16-token blocks, "
@@ -429,6 +435,9 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         "ms_per_launch": ms, "gbs": k1_bytes / (ms * 1e-3) / 1e9,
         "frac_of_hbm_peak": k1_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
         "algorithmic_bytes_per_launch": k1_bytes,
+        "ms_per_launch_eager": ms_eager,
+        "timing": "CUDA graph of 40 launches over the 4 batches; eager: CUDA events around 40 "
+                  "back-to-back binding calls",
     }
     # ---- the same scatter fused with RoPE of Q (32 heads) and K ----
     from workloads.generators import rope_cos_sin_table
@@ -445,7 +454,12 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         it[0] += 1
     for _ in range(8):
         rope_k1()
-    ms = event_time(rope_k1, 40, stream)
+    ms_rope_eager = event_time(rope_k1, 40, stream)
+
+    def rope_b(b):
+        kn, vn, slots = batches[b]
+        pkv.rope_reshape_and_cache(pos, qs[b], kn, vn, kc, vc, slots, table, D)
+    ms = graph_time([functools.partial(rope_b, c % 4) for c in range(40)])
     rope_bytes = T * (2 * H * D * 2 + 2 * (2 * Hkv * D * 2) + D * 4 + 16)
     # the same kernel at a decode step's size: 64 tokens (the staged form),
     # graph-timed since a call's host work outlasts the kernel
@@ -466,6 +480,9 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
                            "table row 512, position + slot 16",
         "ms_per_launch_64_tokens": ms64,
         "timing_64_tokens": "CUDA graph of 100 launches over 4 batches (L2-warm inputs)",
+        "ms_per_launch_eager": ms_rope_eager,
+        "timing": "CUDA graph of 40 launches over the 4 batches; eager: CUDA events around 40 "
+                  "back-to-back binding calls",
     }
     del kc, vc, batches, qs, table
     torch.cuda.empty_cache()
@@ -813,6 +830,8 @@ def main():
                     help="primary timed steps only (no e2e, secondary or CPU legs), for ncu")
     ap.add_argument("--profile-prefill", action="store_true",
                     help="only --steps calls of the 512-token chunk (rotating placements), for ncu")
+    ap.add_argument("--profile-rope", action="store_true",
+                    help="only --steps calls of the fused RoPE + cache write at 8192 tokens, for ncu")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -836,6 +855,34 @@ def main():
         dist.init_process_group("nccl", device_id=device)
     hbm_peak, bf16_peak, bf16_sust, peak_kind = peaks()
     stream = torch.cuda.current_stream()
+    if args.profile_rope:
+        from workloads.generators import random_block_placement, rope_cos_sin_table
+        T, H, Hkv, D = 8192, 32, 8, 128
+        g = torch.Generator(device=device)
+        g.manual_seed(127)
+        nbk = 4 * T // 16 + 64
+        kc = torch.empty((nbk, 16, Hkv, D), dtype=torch.bfloat16, device=device)
+        vc = torch.empty_like(kc)
+        table = rope_cos_sin_table(131072, D).to(device)
+        pos = torch.from_numpy(np.concatenate([np.arange(a, a + 2048)
+                                               for a in (0, 2048, 30000, 120000)])).to(device)
+        batches = []
+        for b in random_block_placement(nbk, [T // 16] * 4, "bench", "k1 8192"):
+            b = b.astype(np.int64)
+            slots = torch.from_numpy((b[:, None] * 16 + np.arange(16)[None, :]).reshape(-1)).to(device)
+            batches.append((torch.randn((T, H, D), generator=g, device=device).to(torch.bfloat16),
+                            torch.randn((T, Hkv, D), generator=g, device=device).to(torch.bfloat16),
+                            torch.randn((T, Hkv, D), generator=g, device=device).to(torch.bfloat16),
+                            slots))
+        err = torch.zeros(1, dtype=torch.int32, device=device)
+        for i in range(args.warmup + args.steps):
+            q, k, v, slots = batches[i % 4]
+            pkv.rope_reshape_and_cache(pos, q, k, v, kc, vc, slots, table, D, error_word=err)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_rope_calls": args.warmup + args.steps,
+                          "error_word": int(err.item())}))
+        return
+
     if args.profile_prefill:
         chunks = build_prefill_chunks(pkv, device)
         for i in range(args.warmup + args.steps):
