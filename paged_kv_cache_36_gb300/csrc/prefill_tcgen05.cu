@@ -34,7 +34,9 @@
 // warp 2 issues PV; warps 4-11 run the softmax and the epilogue.  Each
 // issuer blocks on its own barriers, so neither waits behind the other.
 // Tiles are handed out persistently by a device-side plan over
-// query_start_loc.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
+// query_start_loc, heaviest (most keys) first, in rows of one tile per
+// cluster that alternate direction, so clusters end close together when a
+// prompt's tiles grow from a few key tiles to many.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
 // an abort flag that stops all roles.
 //
 // K/V sharing across a cluster.  With a cluster of C CTAs, the members take C
@@ -172,6 +174,15 @@ __device__ __forceinline__ Tile decode_tile(int ct, int rank, const int32_t* pre
   return t;
 }
 
+// The it-th cluster tile of cluster cid, or -1 when there is none.  Within a
+// request later query tiles see more keys, so tiles are taken from the
+// highest index down, ncl at a time, in alternating direction: each cluster
+// starts with one of the heaviest tiles and heavy and light ones pair up.
+__device__ __forceinline__ int cluster_tile(int it, int cid, int ncl, int total) {
+  const int lin = it * ncl + ((it & 1) ? ncl - 1 - cid : cid);
+  return lin < total ? total - 1 - lin : -1;
+}
+
 // All lanes of the calling warp wait; the result is made warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           volatile int* abort) {
@@ -290,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = smem + (is_k ? L::kK : L::kV);
     uint32_t q_uses = 0, count = 0;
     bool ok = true;
-    for (int ct = cid; ct < total && ok; ct += ncl) {
+    for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0 && ok;
+         ct = cluster_tile(++it, cid, ncl, total)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
       const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
@@ -390,7 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + L::kK), 16, NDH * 1024);
       uint32_t q_count = 0, k_count = 0, s_count = 0;
       bool ok = true;
-      for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
+      for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0 && ok && !*abort_flag;
+           ct = cluster_tile(++it, cid, ncl, total)) {
         const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
         ok = mbar_wait_or_abort(&bars[kQFull], q_count & 1, p.err, abort_flag);
         ++q_count;
@@ -431,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + L::kV), 1024, NDH * 1024);
       uint32_t v_count = 0, s_count = 0;
       bool ok = true;
-      for (int ct = cid; ct < total && ok && !*abort_flag; ct += ncl) {
+      for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0 && ok && !*abort_flag;
+           ct = cluster_tile(++it, cid, ncl, total)) {
         const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
         for (int j = 0; j < t.nkt && ok; ++j) {
           const int vs = v_count % kVStages;
@@ -492,7 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pair_uses;
       return done ? slot[(half ^ 1) * 128 + row] : mine;
     };
-    for (int ct = cid; ct < total; ct += ncl) {
+    for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0;
+         ct = cluster_tile(++it, cid, ncl, total)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
       const int u = t.u0 + row / G;  // token of this row within the request
