@@ -408,41 +408,72 @@ __global__ void __launch_bounds__(288, 1)
       if (last) {
         __threadfence();
         if (lane == 0) *ctr = 0;  // every split has arrived: ready for the next call
-        __nv_bfloat16* orow = p.out + tok * p.out_stride;
-        for (int g = 0; g < G; ++g) {
-          const int64_t hh = h * G + g;
-          float mx = -INFINITY;
-          for (int s = lane; s < nsplit; s += 32)
-            mx = fmaxf(mx, __ldcg(p.part_ml + ((cfirst + s + r) * p.num_heads + hh) * 2));
+        // Each lane merges one slice of one head: lph lanes per head, dpl
+        // dims each, so every head's partials are read at once and the
+        // loads of kBatch splits are in flight together (merging one head
+        // and one split at a time left its CTA behind the others by the
+        // sum of those load latencies).
+        constexpr int kMaxV = NT * D / 16;  // float4s per lane at most
+        constexpr int kBatch = 4;
+        int gp = 1;
+        while (gp < G) gp <<= 1;
+        const int lph = (32 / gp) < (D / 4) ? (32 / gp) : (D / 4);  // lanes per head
+        const int dpl = D / lph;                                      // dims per lane
+        const int nv = dpl / 4;
+        const int g = lane / lph, sub = lane - g * lph;
+        const bool active = g < G;
+        const int64_t hh = static_cast<int64_t>(h) * G + (active ? g : 0);
+        float mx = -INFINITY;
+        for (int s0 = 0; s0 < nsplit; s0 += 8) {
+          float mv[8];
 #pragma unroll
-          for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          float acc[D / 32];
+          for (int k = 0; k < 8; ++k)
+            mv[k] = s0 + k < nsplit
+                        ? __ldcg(p.part_ml + ((cfirst + s0 + k + r) * p.num_heads + hh) * 2)
+                        : -INFINITY;
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-          float den = 0.f;
-          for (int s0 = 0; s0 < nsplit; s0 += 32) {
-            const int s = s0 + lane;
-            float w = 0.f, lw = 0.f;
-            if (s < nsplit) {
-              const float* ml = p.part_ml + ((cfirst + s + r) * p.num_heads + hh) * 2;
-              w = exp2_approx(__ldcg(ml) - mx);
-              lw = w * __ldcg(ml + 1);
-            }
-            den += lw;
-            const int cnt = nsplit - s0 < 32 ? nsplit - s0 : 32;
-            for (int k = 0; k < cnt; ++k) {
-              const float wk = __shfl_sync(0xffffffffu, w, k);
-              const float* po = p.part_o + ((cfirst + s0 + k + r) * p.num_heads + hh) * D;
+          for (int k = 0; k < 8; ++k) mx = fmaxf(mx, mv[k]);
+        }
+        float4 acc[kMaxV];
 #pragma unroll
-              for (int i = 0; i < D / 32; ++i) acc[i] += wk * __ldcg(po + lane + 32 * i);
+        for (int v = 0; v < kMaxV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
+        for (int s0 = 0; s0 < nsplit; s0 += kBatch) {
+          float w[kBatch];
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) {
+            w[k] = 0.f;
+            if (s0 + k < nsplit) {
+              const float* ml = p.part_ml + ((cfirst + s0 + k + r) * p.num_heads + hh) * 2;
+              w[k] = exp2_approx(__ldcg(ml) - mx);
+              den += w[k] * __ldcg(ml + 1);
             }
           }
 #pragma unroll
-          for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-          const float inv = 1.f / den;
-          __nv_bfloat16* dst = orow + hh * D;
+          for (int k = 0; k < kBatch; ++k) {
+            if (s0 + k >= nsplit) break;
+            const float4* po = reinterpret_cast<const float4*>(
+                p.part_o + ((cfirst + s0 + k + r) * p.num_heads + hh) * D + sub * dpl);
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) dst[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+            for (int v = 0; v < kMaxV; ++v) {
+              if (v < nv) {
+                const float4 x4 = __ldcg(po + v);
+                acc[v].x += w[k] * x4.x;
+                acc[v].y += w[k] * x4.y;
+                acc[v].z += w[k] * x4.z;
+                acc[v].w += w[k] * x4.w;
+              }
+            }
+          }
+        }
+        if (active) {
+          const float inv = 1.f / den;
+          uint2* dst = reinterpret_cast<uint2*>(p.out + tok * p.out_stride + hh * D + sub * dpl);
+#pragma unroll
+          for (int v = 0; v < kMaxV; ++v)
+            if (v < nv)
+              dst[v] = make_uint2(pack_bf16(acc[v].x * inv, acc[v].y * inv),
+                                  pack_bf16(acc[v].z * inv, acc[v].w * inv));
         }
       }
     }
