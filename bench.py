@@ -521,6 +521,18 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         res_copy[name] = {"ms": ms, "gbs": copy_bytes / (ms * 1e-3) / 1e9}
     res_copy["device_to_device"]["frac_of_hbm_peak"] = \
         2 * copy_bytes / (res_copy["device_to_device"]["ms"] * 1e-3) / 1e9 / hbm_peak
+    # the link's own rate: the copy engines moving the same bytes contiguously
+    dk, dv = kc[:n], vc[:n]
+    link = {}
+    for name, fn in (("device_to_host", lambda: (hk.copy_(dk, non_blocking=True),
+                                                 hv.copy_(dv, non_blocking=True))),
+                     ("host_to_device", lambda: (dk.copy_(hk, non_blocking=True),
+                                                 dv.copy_(hv, non_blocking=True)))):
+        for _ in range(3):
+            fn()
+        link[name] = copy_bytes / (event_time(fn, 10, stream) * 1e-3) / 1e9
+        res_copy[name]["link_memcpy_gbs"] = link[name]
+        res_copy[name]["frac_of_link"] = res_copy[name]["gbs"] / link[name]
     res["copy_blocks"] = res_copy
     del kc, vc, hk, hv
     torch.cuda.empty_cache()
