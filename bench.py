@@ -1029,6 +1029,12 @@ def main():
                "kind": "oracle", "cpu_model": cpu_model(),
                "sample": f"{n} requests of the headline batch in rotation ({dt:.1f} s): "
                          f"reshape_and_cache scatter of the new token + float64 attention"}
+        # the same oracle on one core, over a shorter sample
+        torch.set_num_threads(1)
+        nb1, dt1, n1 = o.sample(4.0)
+        cpu["single_thread"] = {"value": nb1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                                "sample": f"{n1} requests ({dt1:.1f} s)"}
+        torch.set_num_threads(os.cpu_count() or 1)
 
     if rank == 0:
         clk = clocks.summary()

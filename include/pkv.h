@@ -17,6 +17,13 @@
  *     cudaStream_t passed as `void* stream` (NULL = the legacy default
  *     stream).  They enqueue work asynchronously, never synchronise the
  *     stream and never allocate or free device memory.
+ *   - Validation: with PKV_VALIDATE=1 in the environment, a device entry
+ *     point that has an error word (the attention workspace's word 0, or
+ *     the error_word argument when it is not NULL) waits for its stream
+ *     after launching, reads that word (one device-to-host copy) and returns
+ *     PKV_E_INVALID, naming the bits, if any is set.  The word is cumulative,
+ *     so once set every later validated call fails until the caller clears
+ *     it.  Off by default: no call then synchronises.
  *   - Host entry points (allocator, scheduler, metadata) take HOST pointers;
  *     opaque handles are owned by the library and released by *_destroy.
  *   - Float tensors are all float32 (PKV_F32) or all bfloat16 (PKV_BF16)

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "kernels.h"
@@ -151,6 +152,27 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(PKV_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// PKV_VALIDATE=1 in the environment: after its launches an entry point waits
+// for its stream, reads its device error word (one device-to-host copy) and
+// turns any PKV_ERR_* bit into PKV_E_INVALID.  Off by default, so no call
+// synchronises.
+bool validate_enabled() {
+  const char* v = std::getenv("PKV_VALIDATE");
+  return v && v[0] == '1';
+}
+
+int validate_error_word(const uint32_t* word, cudaStream_t stream, const char* where) {
+  if (!word || !validate_enabled()) return PKV_OK;
+  uint32_t bits = 0;
+  cudaError_t e = cudaMemcpyAsync(&bits, word, sizeof(bits), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, where);
+  if (bits)
+    return fail(PKV_E_INVALID, "%s: the kernels reported error bits 0x%x (1 block id, 2 slot, "
+                "4 metadata, 8 timeout, 16 position)", where, bits);
+  return PKV_OK;
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -186,7 +208,8 @@ int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride
                                            key_cache, value_cache, slot_mapping, num_tokens,
                                            num_blocks * block_size, row_bytes, error_word,
                                            static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "reshape_and_cache launch");
+  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  return validate_error_word(error_word, static_cast<cudaStream_t>(stream), "reshape_and_cache");
 }
 
 int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t query_stride,
@@ -248,7 +271,8 @@ int pkv_rope_reshape_and_cache(const int64_t* positions, void* query, int64_t qu
   a.bf16 = dtype == PKV_BF16;
   a.err = error_word;
   cudaError_t e = launch_rope_reshape_and_cache(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "rope_reshape_and_cache launch");
+  if (e != cudaSuccess) return cuda_fail(e, "rope_reshape_and_cache launch");
+  return validate_error_word(error_word, static_cast<cudaStream_t>(stream), "rope_reshape_and_cache");
 }
 
 int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void* dst_key_cache,
@@ -268,7 +292,8 @@ int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void
                                      dst_value_cache, block_pairs, num_pairs, block_bytes,
                                      src_num_blocks, dst_num_blocks, error_word,
                                      static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "copy_blocks launch");
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return validate_error_word(error_word, static_cast<cudaStream_t>(stream), "copy_blocks");
 }
 
 size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_t head_dim) {
@@ -276,7 +301,7 @@ size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_
   return workspace_layout(num_reqs, num_heads, head_dim, current_grid()).total;
 }
 
-int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_cache,
+static int paged_attention_launch(const void* q, int64_t q_stride, const void* key_cache,
                                const void* value_cache, const int32_t* block_table,
                                int32_t block_table_stride, const int32_t* query_start_loc,
                                const int32_t* seq_lens, const int32_t* num_computed_tokens,
@@ -377,6 +402,25 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
   e = launch_decode_bf16(a, kblk, vblk, ds, grid, prefill, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
+}
+
+int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_cache,
+                               const void* value_cache, const int32_t* block_table,
+                               int32_t block_table_stride, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                               float scale, void* out, int64_t out_stride, int64_t num_tokens,
+                               int32_t num_reqs, int64_t num_blocks, int32_t block_size,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t dtype, int32_t max_query_len, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  const int rc = paged_attention_launch(
+      q, q_stride, key_cache, value_cache, block_table, block_table_stride, query_start_loc,
+      seq_lens, num_computed_tokens, scale, out, out_stride, num_tokens, num_reqs, num_blocks,
+      block_size, num_heads, num_kv_heads, head_dim, dtype, max_query_len, workspace,
+      workspace_bytes, stream);
+  if (rc != PKV_OK || num_tokens == 0 || num_reqs == 0) return rc;
+  return validate_error_word(static_cast<const uint32_t*>(workspace),
+                             static_cast<cudaStream_t>(stream), "paged_attention_varlen");
 }
 
 }  // extern "C"

@@ -133,6 +133,46 @@ def test_tiny_mixed_step(dtype):
     compare(b.attention(), b.oracle(), b.qsl_host, dtype)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_tiny_alternative_readings(dtype):
+    """The other readings of the tiny configuration: (a) request 0 holds 40
+    cached tokens and decodes at position 40 (slot 200); (b) request 1's last
+    7 of 20 tokens run in chunks (13,16), (16,19), (19,20) over 13 cached
+    ones, and their concatenated outputs equal one 7-token chunk."""
+    case = configs.tiny_fp32_case(dtype)
+    h, hkv, d = case.num_heads, case.num_kv_heads, case.head_dim
+    # (a) a 41-token history for request 0
+    k41 = randn_fp32((41, hkv, d), "tiny_alt", "k", dtype=dtype)
+    v41 = randn_fp32((41, hkv, d), "tiny_alt", "v", dtype=dtype)
+    q41 = randn_fp32((1, h, d), "tiny_alt", "q", dtype=dtype)
+    kv = KVHistory(k41, v41, np.array([41], np.int64), np.array([0], np.int64))
+    b = Batch(kv, [np.array([5, 8, 12], np.int32)], case.num_blocks, [1], [40], q41, h, dtype)
+    b.alloc_cache().fill_history().upload_metadata()
+    assert b.slot_mapping.tolist() == [200]
+    b.write_new_tokens()
+    compare(b.attention(), b.oracle(), b.qsl_host, dtype)
+    # (b) chunks over request 1's positions [13, 20)
+    shape = (case.num_blocks, 16, hkv, d)
+    kc = torch.empty(shape, dtype=dtype, device="cuda")
+    vc = torch.empty_like(kc)
+    outs = []
+    for i, (a, e) in enumerate([(13, 16), (16, 19), (19, 20)]):
+        bb = _tiny_batch(case, [1], [e - a], [a], dtype)
+        bb.key_cache, bb.value_cache = kc, vc
+        if i == 0:
+            bb.fill_history()                              # positions 0..12
+        bb.upload_metadata()
+        assert bb.slot_mapping.tolist() == {13: [61, 62, 63], 16: [112, 113, 114], 19: [115]}[a]
+        bb.write_new_tokens()
+        outs.append(bb.attention().clone())
+        compare(outs[-1], bb.oracle(), bb.qsl_host, dtype)
+    whole = _tiny_batch(case, [1], [7], [13], dtype).alloc_cache().fill_history()
+    whole.upload_metadata().write_new_tokens()
+    ref = whole.oracle()
+    compare(torch.cat(outs), ref, whole.qsl_host, dtype)
+    compare(whole.attention(), ref, whole.qsl_host, dtype)
+
+
 # ---------------------------------------------------------------- random varlen batches
 CASES = [
     # (H, Hkv, D, query lens, num_computed) - several tiles, ragged tails, empty requests
@@ -306,3 +346,25 @@ def test_config4_long_decode_llama70b():
     b = _decode_cfg_batch(cfg).alloc_cache().fill_history().upload_metadata().write_new_tokens()
     out = b.attention()
     compare(out, b.oracle(), b.qsl_host, torch.bfloat16)
+
+
+def test_validate_mode_reports_kernel_error_bits(monkeypatch):
+    """PKV_VALIDATE=1: an inconsistent seq_len (metadata error bit) makes the
+    call itself fail; without it the call succeeds and the bit waits in the
+    error word."""
+    pkv = _pkv()
+    case = configs.tiny_fp32_case(torch.bfloat16)
+    b = _tiny_batch(case, [0, 1], [1, 1], [39, 19], torch.bfloat16).alloc_cache().fill_history()
+    b.upload_metadata().write_new_tokens()
+    monkeypatch.setenv("PKV_VALIDATE", "1")
+    b.attention()                                          # consistent: passes validation
+    b.seq_lens[1] += 5                                     # seq_len != num_computed + 1
+    ws = pkv.new_workspace(b.R, b.H, b.D)
+    with pytest.raises(pkv.PkvError, match="error bits 0x4"):
+        pkv.paged_attention_varlen(b.q, b.key_cache, b.value_cache, b.block_table, b.qsl,
+                                   b.seq_lens, b.nc, 0.125, workspace=ws, max_query_len=1)
+    monkeypatch.delenv("PKV_VALIDATE")
+    ws = pkv.new_workspace(b.R, b.H, b.D)
+    pkv.paged_attention_varlen(b.q, b.key_cache, b.value_cache, b.block_table, b.qsl,
+                               b.seq_lens, b.nc, 0.125, workspace=ws, max_query_len=1)
+    assert pkv.read_error_word(ws) & pkv.ERR_METADATA

@@ -153,3 +153,13 @@ def test_delta_blocks_telescopes(B):
             total += d
             held += s
             assert total == math.ceil(held / B) == _simulate_blocks(held, B)
+
+
+def test_tiny_config_alternative_readings():
+    """The readings the tiny configuration also runs as extra tests: request 0
+    with 40 cached tokens and its decode query at position 40 (slot 200), and
+    request 1's last 7 of 20 tokens in chunks (13,16), (16,19), (19,20)."""
+    assert paging.slot_index([5, 8, 12], 40, 16) == 12 * 16 + 8 == 200
+    rows = [[3, 7]]
+    got = [paging.slot_mapping(rows, [e - a], [a], 16) for a, e in [(13, 16), (16, 19), (19, 20)]]
+    assert got == [[61, 62, 63], [112, 113, 114], [115]]
