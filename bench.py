@@ -334,6 +334,20 @@ def graph_time(calls, reps=5):
     return statistics.median(times)
 
 
+def combine_ranks(ms: float, units: float, dist=None, device="cpu") -> tuple[float, float]:
+    """Whole-job figures of a replicas run: the slowest rank's time and the
+    units (bytes or tokens) all ranks processed.  Every rank runs its own
+    replica, so this is the only exchange; without a process group the
+    rank's own figures come back unchanged."""
+    if dist is None:
+        return ms, units
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def cpu_model() -> str:
     """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
     try:
@@ -916,14 +930,12 @@ def main():
         total_ms, attn_ms = time_loop(steps, args.steps, stream, per_call=True)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+    step_bytes = steps[0].attn_bytes + steps[0].k1_bytes
+    total_ms, job_bytes = combine_ranks(total_ms, float(step_bytes) * args.steps, dist, device)
     if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
     ms_per_step = total_ms / args.steps
-    step_bytes = steps[0].attn_bytes + steps[0].k1_bytes
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = job_bytes / (total_ms * 1e-3) / 1e9
     attn_avg_ms = statistics.mean(attn_ms)
     decode_gbs = steps[0].decode_bytes / (attn_avg_ms * 1e-3) / 1e9
     traffic = traffic_from_profile("decode_splitkv", ["decode_splitkv.cu"], 1.0)
@@ -977,7 +989,8 @@ def main():
     for _ in range(e2e_n):
         e2e_step()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_n
-    e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
+    e2e_ms, e2e_bytes = combine_ranks(e2e_ms, float(step_bytes), dist, device)
+    e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
 
     # ---- secondary: the mixed chunked-prefill step ----
     secondary = None
@@ -989,14 +1002,14 @@ def main():
             chunks[i % len(chunks)].attn()
         n2 = max(20, min(args.steps // 10, 300))
         tot, _ = time_loop([mstep], n2, stream)
-        mixed_ms = tot / n2
+        mixed_ms, mixed_tokens = combine_ranks(tot / n2, float(mstep.T), dist, device)
         # one call per placement, each a decode launch with no rows plus the
         # prefill kernel (launched as its programmatic dependent)
         chunk_ms = graph_time([c.attn for c in chunks] * 5)
         chunk_tflops = mstep.prefill_flops / (chunk_ms * 1e-3) / 1e12
         secondary = {
             "metric": "mixed-batch attention tokens/s/layer",
-            "value": mstep.T * world / (mixed_ms * 1e-3), "unit": "tokens/s/layer",
+            "value": mixed_tokens / (mixed_ms * 1e-3), "unit": "tokens/s/layer",
             "ms_per_step": mixed_ms,
             "workload": "512-token prefill chunk at [1536,2048) + 256 decodes (ctx U[256,8192]), "
                         "Llama-3-8B heads, 131072-block pool",
