@@ -196,6 +196,13 @@ int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void
  *   requests (its layout follows the largest batch it can hold).  Word 0 is
  *   the error word (PKV_ERR_* bits, OR-ed in).  Two calls that overlap on the
  *   GPU must not share a workspace.
+ * Ordering: the kernels are launched as programmatic dependents of the
+ * kernel before the call on `stream`, so their set-up overlaps its tail.
+ * They read q and the caches and write out and the workspace only after that
+ * kernel has completed (reshape_and_cache may come directly before).  The
+ * metadata arrays (block_table, query_start_loc, seq_lens,
+ * num_computed_tokens) are read earlier: fill them by copies or kernels that
+ * come before that kernel, not by the kernel directly before the call.
  * ---------------------------------------------------------------------- */
 size_t pkv_attention_workspace_bytes(int32_t num_reqs, int32_t num_heads, int32_t head_dim);
 

@@ -379,12 +379,16 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   ds.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   ds.part_o = reinterpret_cast<float*>(ws + wl.part_o);
   ds.num_slots = wl.slots;
-  // Rows with query length > 1 go to the prefill kernel, launched first (a
-  // normal launch: it reads what reshape_and_cache wrote).  The decode kernel
-  // follows as its programmatic dependent: it reads nothing the prefill
-  // writes, so it is scheduled onto SMs as they free up, and with no decode
-  // rows its launch hides behind the prefill.  A decode-only call launches
-  // the decode kernel normally.
+  // Rows with query length > 1 go to the prefill kernel, launched first as a
+  // programmatic dependent of the kernel before it: its set-up and plan read
+  // only metadata, and its copies of Q, K and V wait for that kernel (for
+  // instance reshape_and_cache) to complete.  The decode kernel follows as
+  // the prefill's programmatic dependent, released once the prefill has seen
+  // its predecessor complete; it reads nothing the prefill writes, so it is
+  // scheduled onto SMs as they free up, and with no decode rows its launch
+  // hides behind the prefill.  In a decode-only call the decode kernel is the
+  // programmatic dependent of the kernel before the call and waits for it
+  // before reading Q or the caches.
   const bool prefill = max_query_len != 1;
   cudaError_t e = cudaSuccess;
   if (prefill) {

@@ -96,6 +96,11 @@ __global__ void __launch_bounds__(288, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
 
+  // A kernel launched as this grid's programmatic dependent (the next call's
+  // prefill or decode kernel) may start its metadata-only prologue now; it
+  // touches Q, the caches, out and the workspace only after this grid has
+  // completed.
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int hkv = p.hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = p.num_reqs;
@@ -169,9 +174,9 @@ __global__ void __launch_bounds__(288, 1)
     // Launched as a programmatic dependent, this grid may run its prologue
     // while the kernel before it finishes.  When that kernel may be the cache
     // write (with or without RoPE, which also rewrites Q), the caches and Q
-    // are read only after it has completed; after the prefill kernel (which
-    // writes nothing this grid reads and started after the cache write
-    // completed) there is nothing to wait for here.
+    // are read only after it has completed.  After the prefill kernel there
+    // is nothing to wait for here: it writes nothing this grid reads, and it
+    // releases this grid only once it has seen the cache write complete.
     if (p.wait_before_loads) grid_dependency_wait();
     int stage = 0;
     uint32_t phase = 0;

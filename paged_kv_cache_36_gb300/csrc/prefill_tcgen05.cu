@@ -237,9 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // each role waits only just before its first cross-CTA operation, so the
   // members' launch skew overlaps the plan and the first local copies.
   if (C > 1) cluster_arrive_release();
-  // the decode kernel launched after this one reads nothing it writes: let it
-  // be scheduled onto SMs as they free up
-  if (threadIdx.x == 0) grid_launch_dependents();
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -286,6 +283,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 3) {
+    // This grid is a programmatic dependent of the kernel before it, so the
+    // set-up and plan above (metadata only) overlap that kernel's tail.  Q
+    // and the caches may be written by it (the cache write, with RoPE also
+    // Q), so the copies start only after it has completed.  Every thread
+    // that writes global memory does so after data these copies brought.
+    grid_dependency_wait();
+    // Let the decode kernel of this call be scheduled only now: it reads the
+    // caches and Q without waiting for this grid, which is safe once the
+    // cache write before this grid is known to be complete.
+    if (warp == 0 && lane == 0) grid_launch_dependents();
     // ============================ TMA producers ============================
     // warp 0 streams Q and K, warp 3 streams V.  They are separate warps so
     // that neither waits on the other's ring: two lanes of one warp would run
@@ -715,17 +722,21 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap&
   });
   if (info.status[dev] != cudaSuccess) return info.status[dev];
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // a programmatic dependent of the kernel before it in the stream (see the
+  // wait at the top of the producer warps)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(info.clusters[dev] * C));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, prm);
 }
 
