@@ -382,7 +382,8 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     """Supporting measurements beside the headline: the long-context decode
     (config 4), the continuous-batching trace (config 5) per step,
     reshape_and_cache at 8192 tokens with and without the fused RoPE of Q and
-    K, and the prefill kernel on a 2048-token prompt."""
+    K, and the prefill kernel on a 2048-token prompt, on 8 such prompts in one
+    call and on one 16384-token prompt."""
     from workloads import configs, trace_spec, generate_arrivals
     from workloads.generators import random_block_placement
     res = {}
@@ -512,6 +513,34 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     }
     del prompts
     torch.cuda.empty_cache()
+    # ---- the prefill kernel where its start and end are amortised: many
+    # tiles per CTA (8 prompts of 2048 tokens in one call) and one long
+    # prompt (16384 tokens, causal tiles of 1 to 128 key tiles) ----
+    for key, nreq, plen in (("prefill_8x2048", 8, 2048), ("prefill_16384", 1, 16384)):
+        copies = 4
+        nblk = plen // 16
+        pool = nreq * nblk * copies
+        places = random_block_placement(pool, [nblk] * (nreq * copies), "bench", key)
+        kc = torch.randn((pool, 16, 8, 128), generator=g, device=device).to(torch.bfloat16)
+        vc = torch.randn((pool, 16, 8, 128), generator=g, device=device).to(torch.bfloat16)
+        calls = []
+        for c in range(copies):
+            q = torch.randn((nreq * plen, 32, 128), generator=g, device=device).to(torch.bfloat16)
+            calls.append(DeviceStep(pkv, kc, vc, q, q[:0, :8], q[:0, :8],
+                                    places[c * nreq:(c + 1) * nreq], np.full(nreq, plen),
+                                    np.zeros(nreq, np.int64), 32, device))
+        ms = graph_time([c.attn for c in calls] * 2)
+        fl = calls[0].prefill_flops
+        res[key] = {
+            "workload": f"{nreq} prompt(s) of {plen} tokens from an empty cache in one call, "
+                        f"Llama-3-8B heads, {copies} rotating placements "
+                        f"({copies * nreq * plen * 4096 / 1e6:.0f} MB of K/V; graph-timed)",
+            "ms_per_call": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / bf16_peak, "flops": fl,
+            "error_word": pkv.read_error_word(calls[0].ws),
+        }
+        del calls, kc, vc, q
+        torch.cuda.empty_cache()
     # ---- whole-block copies: copy-on-write within the pool, offload to and
     # reload from pinned host memory (the GPU drives the CPU-GPU link) ----
     nbp, n = 16384, 4096
