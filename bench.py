@@ -4,7 +4,9 @@
 
 One step is one pass of the hot path over one batch that is already resident
 in HBM: reshape_and_cache of the step's new tokens, then paged attention over
-the whole batch.  The headline workload is the Llama-3-8B decode batch (64
+the whole batch, made as one call (reshape_and_cache_paged_attention), which
+for this decode-only batch is one kernel; the same steps as two calls are
+reported beside it (`step_forms`).  The headline workload is the Llama-3-8B decode batch (64
 requests, one query each, contexts uniform on [128, 4096], 32/8/128 heads,
 block_size 16, blocks drawn from a 65536-block pool).  It is reported as
 algorithmic HBM bytes per second:
@@ -177,6 +179,7 @@ class DeviceStep:
         self.slots = torch.from_numpy(self.slots_host).to(device)
         self.out = torch.empty_like(self.q)
         self.ws = pkv.new_workspace(self.R, self.H, self.D, device)
+        self.fuse = False
         self.max_q = int(qlens.max())
         self.scale = 1.0 / math.sqrt(self.D)
         self.T = int(qlens.sum())
@@ -204,9 +207,19 @@ class DeviceStep:
                                         self.seq_lens, self.nc, self.scale, out=self.out,
                                         workspace=self.ws, max_query_len=self.max_q)
 
+    def fused(self):
+        """reshape_and_cache + attention in one call (one kernel for a decode-only step)."""
+        self.pkv.reshape_and_cache_paged_attention(
+            self.k_new, self.v_new, self.slots, self.q, self.kc, self.vc, self.block_table,
+            self.qsl, self.seq_lens, self.nc, self.scale, out=self.out, workspace=self.ws,
+            max_query_len=self.max_q)
+
     def step(self):
-        self.k1()
-        self.attn()
+        if self.fuse:
+            self.fused()
+        else:
+            self.k1()
+            self.attn()
 
 
 def build_decode_steps(pkv, device, replicas=4):
@@ -765,7 +778,8 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
 
 def time_loop(fn_list, steps, stream, per_call=None):
     """Runs fn_list[i % len] for `steps` iterations between two events; if
-    per_call is given, also brackets that callable with events each step.
+    per_call is given, also brackets the attention launch with events each
+    step (the whole step when it is one fused call).
     Returns (total ms, [per-call ms])."""
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     marks = []
@@ -775,10 +789,14 @@ def time_loop(fn_list, steps, stream, per_call=None):
         if per_call is None:
             s.step()
         else:
-            s.k1()
+            if not s.fuse:
+                s.k1()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            s.attn()
+            if s.fuse:
+                s.fused()
+            else:
+                s.attn()
             b.record(stream)
             marks.append((a, b))
     end.record(stream)
@@ -948,6 +966,8 @@ def main():
         return
 
     cfg, steps = build_decode_steps(pkv, device)
+    for s in steps:  # the cache write and the attention as one kernel
+        s.fuse = True
     for i in range(args.warmup):
         steps[i % len(steps)].step()
     torch.cuda.synchronize()
@@ -956,7 +976,7 @@ def main():
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        total_ms, attn_ms = time_loop(steps, args.steps, stream, per_call=True)
+        total_ms, _ = time_loop(steps, args.steps, stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     step_bytes = steps[0].attn_bytes + steps[0].k1_bytes
@@ -965,9 +985,36 @@ def main():
         dist.barrier()
     ms_per_step = total_ms / args.steps
     value = job_bytes / (total_ms * 1e-3) / 1e9
-    attn_avg_ms = statistics.mean(attn_ms)
-    decode_gbs = steps[0].decode_bytes / (attn_avg_ms * 1e-3) / 1e9
+    # One kernel per step, launched back to back on `stream`: the events
+    # around the K launches give its average launch time.  Consecutive
+    # launches overlap only in the next launch's metadata prologue (its
+    # loads wait for the previous grid to complete).
+    attn_avg_ms = total_ms / args.steps
+    # the fused kernel's algorithmic bytes: the decode reads plus the cache write
+    kernel_bytes = steps[0].decode_bytes + steps[0].k1_bytes
+    decode_gbs = kernel_bytes / (attn_avg_ms * 1e-3) / 1e9
     traffic = traffic_from_profile("decode_splitkv", ["decode_splitkv.cu"], 1.0)
+    # the same steps as two calls (reshape_and_cache, then attention), as one
+    # call again, and as one call with events around each launch, for comparison
+    forms = None
+    if not args.profile:
+        forms = {}
+        for fuse, key in ((False, "two_calls_ms_per_step"), (True, "one_call_ms_per_step")):
+            for s in steps:
+                s.fuse = fuse
+            for i in range(args.warmup):
+                steps[i % len(steps)].step()
+            n = max(100, min(args.steps, 2000))
+            tot, _ = time_loop(steps, n, stream)
+            forms[key] = tot / n
+        # each launch bracketed by its own events, which also keeps the next
+        # launch's prologue from overlapping it
+        _, marks = time_loop(steps, n, stream, per_call=True)
+        forms["one_call_isolated_ms"] = statistics.mean(marks)
+        forms["timing"] = ("CUDA events around the whole loop (two_calls, one_call) or around "
+                           "each call (one_call_isolated); same steps and placements")
+        for s in steps:
+            s.fuse = True
 
     if args.profile:
         args.no_secondary = args.no_cpu_baseline = True
@@ -1005,9 +1052,10 @@ def main():
         # a2 on the host: slot_mapping from the block table, then H2D, kernels, D2H
         host["slots"].numpy()[:] = pkv.build_slot_mapping(s0.bt_host, s0.qsl_host, s0.nc_host, 16)
         stage_dev.copy_(stage_host, non_blocking=True)
-        pkv.reshape_and_cache(dev["k_new"], dev["v_new"], s0.kc, s0.vc, dev["slots"])
-        pkv.paged_attention_varlen(dev["q"], s0.kc, s0.vc, dev["bt"], dev["qsl"], dev["seq"],
-                                   dev["nc"], s0.scale, out=s0.out, workspace=s0.ws, max_query_len=1)
+        pkv.reshape_and_cache_paged_attention(
+            dev["k_new"], dev["v_new"], dev["slots"], dev["q"], s0.kc, s0.vc, dev["bt"],
+            dev["qsl"], dev["seq"], dev["nc"], s0.scale, out=s0.out, workspace=s0.ws,
+            max_query_len=1)
         out_host.copy_(s0.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -1094,21 +1142,25 @@ def main():
                 "l2": "inputs larger than L2: steps rotate over 4 disjoint placements (0.55 GB each)",
                 "parallelism": f"replicas x{world}",
             },
-            "roofline": {"kernel": "decode_splitkv_kernel", "bound": "hbm",
+            "roofline": {"kernel": "decode_splitkv_kernel (reshape_and_cache fused)",
+                         "bound": "hbm",
                          "achieved": decode_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": decode_gbs / hbm_peak, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": steps[0].decode_bytes,
+                         "algorithmic_bytes_per_launch": kernel_bytes,
                          "avg_launch_ms": attn_avg_ms,
+                         "timing": "CUDA events on the launching stream around the timed "
+                                   "region's back-to-back launches (one per step)",
                          "traffic": traffic},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "path": "host slot_mapping build into a pinned staging buffer holding all "
-                            "of the step's inputs -> one H2D copy -> reshape_and_cache -> "
-                            "paged_attention_varlen -> D2H out -> stream sync"},
+                            "of the step's inputs -> one H2D copy -> "
+                            "reshape_and_cache_paged_attention -> D2H out -> stream sync"},
             "secondary": secondary,
             "extra": extra,
             "cpu_baseline": cpu,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": args.steps,
+            "step_forms": forms,
             "clocks": clk,
             "wall_s_timed": wall,
         }

@@ -93,6 +93,38 @@ int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride
                           int32_t dtype, uint32_t* error_word, void* stream);
 
 /* ------------------------------------------------------------------------
+ * reshape_and_cache + paged_attention_varlen in one call  [AI Infra,
+ * section "Attention Module": the new K/V go into the paged cache by
+ * slot_mapping, then attention reads every request's history, this step's
+ * tokens included, through block_table]
+ *
+ * Same result as pkv_reshape_and_cache(key, value, ..., slot_mapping, error
+ * word = workspace word 0) followed by pkv_paged_attention_varlen(...) on the
+ * same stream.  key, value: device [num_tokens, num_kv_heads, head_dim] with
+ * token strides key_stride / value_stride (elements, 16-byte multiples);
+ * slot_mapping: device int64 [num_tokens]; every other argument as for
+ * pkv_paged_attention_varlen.
+ * When dtype is PKV_BF16 and max_query_len is 1 (a decode-only step) the two
+ * run as ONE kernel: the CTA that reads a request's last block writes that
+ * token's K and V rows to slot_mapping[token] and uses them in place of the
+ * cache's copy, so the step costs one launch and no read-after-write through
+ * memory.  This requires slot_mapping[token] to be the block table's slot of
+ * position seq_len - 1 (what pkv_build_slot_mapping produces); a token whose
+ * slot differs still has its rows written at slot_mapping[token], and
+ * PKV_ERR_METADATA is set.  Otherwise reshape_and_cache runs as its own
+ * kernel first.
+ * ---------------------------------------------------------------------- */
+int pkv_reshape_and_cache_paged_attention(
+    const void* key, int64_t key_stride, const void* value, int64_t value_stride,
+    const int64_t* slot_mapping, const void* q, int64_t q_stride, void* key_cache,
+    void* value_cache, const int32_t* block_table, int32_t block_table_stride,
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* num_computed_tokens,
+    float scale, void* out, int64_t out_stride, int64_t num_tokens, int32_t num_reqs,
+    int64_t num_blocks, int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t dtype, int32_t max_query_len, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * rope_reshape_and_cache  [AI Infra, section "Attention Module (以标准GQA +
  * RoPE为例)": Q and K are rotated by RoPE after the QKV split, the rotation
  * being a block-diagonal rotation matrix applied element-wise with the row of

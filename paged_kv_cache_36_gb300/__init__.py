@@ -20,7 +20,8 @@ from ._ffi import (ERR_BLOCK_ID, ERR_METADATA, ERR_POSITION, ERR_SLOT, ERR_TIMEO
 __all__ = [
     "PkvError", "lib", "reshape_and_cache", "rope_reshape_and_cache", "copy_blocks",
     "attention_workspace_bytes", "new_workspace",
-    "paged_attention_varlen", "read_error_word", "build_slot_mapping", "Allocator", "Scheduler",
+    "paged_attention_varlen", "reshape_and_cache_paged_attention", "read_error_word",
+    "build_slot_mapping", "Allocator", "Scheduler",
 ]
 
 _lib = None
@@ -178,6 +179,39 @@ def paged_attention_varlen(q, key_cache, value_cache, block_table, query_start_l
         _token_stride(out), T, R, nb, bs, H, hkv, D, _dtype_code(q), int(max_query_len),
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(code, "paged_attention_varlen")
+    return out
+
+
+def reshape_and_cache_paged_attention(key, value, slot_mapping, q, key_cache, value_cache,
+                                      block_table, query_start_loc, seq_lens, num_computed_tokens,
+                                      scale: float, out=None, workspace=None,
+                                      max_query_len: int = 0, stream=None):
+    """reshape_and_cache of key/value [T, Hkv, D] at slot_mapping (int64 [T]),
+    then paged_attention_varlen of q [T, H, D]; one fused kernel for a bf16
+    decode-only step (max_query_len == 1).  Returns out [T, H, D]."""
+    import torch
+    T, H, D = q.shape
+    nb, bs, hkv, _ = key_cache.shape
+    R = int(seq_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = new_workspace(R, H, D, q.device)
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [R, max_blocks] with unit inner stride")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    code = lib().pkv_reshape_and_cache_paged_attention(
+        key.data_ptr(), _token_stride(key), value.data_ptr(), _token_stride(value),
+        slot_mapping.data_ptr(), q.data_ptr(), _token_stride(q), key_cache.data_ptr(),
+        value_cache.data_ptr(), block_table.data_ptr(), block_table.stride(0),
+        query_start_loc.data_ptr(), seq_lens.data_ptr(), num_computed_tokens.data_ptr(),
+        float(scale), out.data_ptr(), _token_stride(out), T, R, nb, bs, H, hkv, D, _dtype_code(q),
+        int(max_query_len), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check(code, "reshape_and_cache_paged_attention")
     return out
 
 

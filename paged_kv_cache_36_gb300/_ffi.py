@@ -66,6 +66,10 @@ SIGNATURES = {
     "pkv_paged_attention_varlen": (C.c_int, [vp, i64, vp, vp, vp, i32, vp, vp, vp, f32, vp, i64,
                                              i64, i32, i64, i32, i32, i32, i32, i32, i32, vp, sz,
                                              vp]),
+    "pkv_reshape_and_cache_paged_attention": (C.c_int, [vp, i64, vp, i64, vp, vp, i64, vp, vp,
+                                                        vp, i32, vp, vp, vp, f32, vp, i64, i64,
+                                                        i32, i64, i32, i32, i32, i32, i32, i32,
+                                                        vp, sz, vp]),
     "pkv_paged_attention_varlen_noalloc": (C.c_int, [vp, i64, vp, vp, vp, i32, vp, vp, vp, f32,
                                                      vp, i64, i64, i32, i64, i32, i32, i32, i32,
                                                      i32, i32, vp, vp]),

@@ -309,7 +309,8 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
                                int32_t num_reqs, int64_t num_blocks, int32_t block_size,
                                int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                int32_t dtype, int32_t max_query_len, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+                               size_t workspace_bytes, void* stream,
+                               const CacheWrite* write = nullptr) {
   if (num_tokens < 0 || num_reqs < 0 || num_blocks <= 0 || num_heads <= 0 || num_kv_heads <= 0)
     return fail(PKV_E_INVALID, "pkv_paged_attention_varlen: bad sizes");
   if (dtype != PKV_F32 && dtype != PKV_BF16)
@@ -337,6 +338,19 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   if (block_table_stride <= 0) return fail(PKV_E_INVALID, "block_table_stride must be positive");
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The cache write of this step's tokens fuses into the decode kernel when
+  // every row is a bf16 decode row; otherwise reshape_and_cache runs first.
+  const bool fuse_write = write && dtype == PKV_BF16 && max_query_len == 1;
+  if (write && !fuse_write) {
+    const int64_t esize = dtype == PKV_F32 ? 4 : 2;
+    cudaError_t e = launch_reshape_and_cache(
+        write->key, write->value, write->key_stride * esize, write->value_stride * esize,
+        const_cast<void*>(key_cache), const_cast<void*>(value_cache), write->slot_mapping,
+        num_tokens, num_blocks * block_size, static_cast<int64_t>(num_kv_heads) * head_dim * esize,
+        reinterpret_cast<uint32_t*>(ws), st);
+    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  }
   AttnArgs a;
   a.q = q;
   a.q_stride = q_stride;
@@ -358,7 +372,6 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   a.head_dim = head_dim;
   a.scale = scale;
   a.err = reinterpret_cast<uint32_t*>(ws);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (dtype == PKV_F32) {
     cudaError_t e = launch_attn_rows(a, false, false, st);
@@ -403,7 +416,7 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
     e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
-  e = launch_decode_bf16(a, kblk, vblk, ds, grid, prefill, st);
+  e = launch_decode_bf16(a, kblk, vblk, ds, grid, prefill, st, fuse_write ? write : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
 }
@@ -425,6 +438,45 @@ int pkv_paged_attention_varlen(const void* q, int64_t q_stride, const void* key_
   if (rc != PKV_OK || num_tokens == 0 || num_reqs == 0) return rc;
   return validate_error_word(static_cast<const uint32_t*>(workspace),
                              static_cast<cudaStream_t>(stream), "paged_attention_varlen");
+}
+
+int pkv_reshape_and_cache_paged_attention(
+    const void* key, int64_t key_stride, const void* value, int64_t value_stride,
+    const int64_t* slot_mapping, const void* q, int64_t q_stride, void* key_cache,
+    void* value_cache, const int32_t* block_table, int32_t block_table_stride,
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* num_computed_tokens,
+    float scale, void* out, int64_t out_stride, int64_t num_tokens, int32_t num_reqs,
+    int64_t num_blocks, int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t dtype, int32_t max_query_len, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  if (num_tokens > 0) {
+    if (!key || !value || !slot_mapping)
+      return fail(PKV_E_INVALID, "pkv_reshape_and_cache_paged_attention: null pointer");
+    const int64_t esize = dtype == PKV_F32 ? 4 : 2;
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (!aligned16(key) || !aligned16(value) || (key_stride * esize) % 16 ||
+        (value_stride * esize) % 16 || (row * esize) % 16)
+      return fail(PKV_E_INVALID,
+                  "pkv_reshape_and_cache_paged_attention: key/value rows, strides and bases must "
+                  "be 16-byte aligned");
+    if (key_stride < row || value_stride < row)
+      return fail(PKV_E_INVALID,
+                  "pkv_reshape_and_cache_paged_attention: token stride shorter than a row");
+  }
+  CacheWrite w;
+  w.key = key;
+  w.value = value;
+  w.key_stride = key_stride;
+  w.value_stride = value_stride;
+  w.slot_mapping = slot_mapping;
+  const int rc = paged_attention_launch(
+      q, q_stride, key_cache, value_cache, block_table, block_table_stride, query_start_loc,
+      seq_lens, num_computed_tokens, scale, out, out_stride, num_tokens, num_reqs, num_blocks,
+      block_size, num_heads, num_kv_heads, head_dim, dtype, max_query_len, workspace,
+      workspace_bytes, stream, &w);
+  if (rc != PKV_OK || num_tokens == 0 || num_reqs == 0) return rc;
+  return validate_error_word(static_cast<const uint32_t*>(workspace),
+                             static_cast<cudaStream_t>(stream), "reshape_and_cache_paged_attention");
 }
 
 }  // extern "C"

@@ -77,6 +77,16 @@ struct DecodeParams {
   int32_t wait_before_loads;  // wait for the preceding grid before reading Q or the caches
   int32_t stages;
   uint32_t stage_bytes;
+  // Fused reshape_and_cache (k_new == nullptr: off).  Each decode token's new
+  // K/V row is written to its slot and patched into the stage of its block.
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int64_t k_new_stride;  // elements per token
+  int64_t v_new_stride;
+  const int64_t* slot_mapping;
+  __nv_bfloat16* key_cache;
+  __nv_bfloat16* value_cache;
+  int64_t num_slots;
 };
 
 // CTA that owns global decode block x when N blocks are split over P CTAs as
@@ -241,6 +251,24 @@ __global__ void __launch_bounds__(288, 1)
     const int j1 = static_cast<int>(seg_end - prefix[r]);
     const int64_t tok = __ldg(p.qsl + r);
     const int seq = __ldg(p.seq_lens + r);
+    // Fused cache write: the segment holding the request's last block takes
+    // this head's new K row (lanes [0, D/8)) and V row (lanes [D/8, D/4)),
+    // one 16-byte chunk per lane, loaded now beside Q.
+    const bool patch = p.k_new != nullptr && seg_end == prefix[r + 1];
+    constexpr int kChunks = D / 8;  // 16-byte chunks in one head's row
+    const bool patch_lane = patch && lane < 2 * kChunks;
+    const bool patch_v = lane >= kChunks;
+    const int patch_chunk = patch_v ? lane - kChunks : lane;
+    uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+    int64_t new_slot = -1, want_slot = -1;
+    if (patch_lane) {
+      const __nv_bfloat16* src = patch_v ? p.v_new + tok * p.v_new_stride
+                                         : p.k_new + tok * p.k_new_stride;
+      new_row = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(h) * D) + patch_chunk);
+      new_slot = __ldg(p.slot_mapping + tok);
+      want_slot = static_cast<int64_t>(__ldg(p.block_table + static_cast<int64_t>(r) * p.bt_stride +
+                                             (seq - 1) / 16)) * 16 + (seq - 1) % 16;
+    }
 
     // B fragments of Q^T: b0 = Q[g][16ks + 2tid .. +1], b1 = Q[g][16ks + 8 + 2tid .. +1]
     uint32_t qb[NT][KS][2];
@@ -274,6 +302,29 @@ __global__ void __launch_bounds__(288, 1)
       uint8_t* vst = kst + kv_region;
       const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
       const int valid = seq - j * 16 < 16 ? seq - j * 16 : 16;
+      if (patch && j == j1 - 1) {
+        // The block of position seq - 1: its row valid - 1 is this step's
+        // token, which the cache may not hold yet.  Use the new row here and
+        // write it to its slot (reshape_and_cache semantics: slot < 0 is
+        // padding, a slot past the pool is skipped and flagged).
+        if (patch_lane) {
+          uint8_t* base = patch_v ? vst : kst;
+          *reinterpret_cast<uint4*>(base + (patch_chunk >> 3) * kBox +
+                                    swz128(valid - 1, patch_chunk & 7)) = new_row;
+          if (new_slot >= 0 && new_slot < p.num_slots) {
+            __nv_bfloat16* dst = (patch_v ? p.value_cache : p.key_cache) +
+                                 new_slot * (static_cast<int64_t>(hkv) * D) +
+                                 static_cast<int64_t>(h) * D;
+            reinterpret_cast<uint4*>(dst)[patch_chunk] = new_row;
+          } else if (new_slot >= p.num_slots) {
+            atomicOr(p.err, PKV_ERR_SLOT);
+          }
+          // the attention used the new row at the block table's slot
+          if (new_slot != want_slot && lane == 0) atomicOr(p.err, PKV_ERR_METADATA);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (valid < 16) {
         // rows past the sequence hold whatever the pool had: zero this head's V rows
         for (int i = lane; i < NDH * (16 - valid) * 8; i += 32) {
@@ -517,7 +568,7 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, const CUtensorMap& k
 
 cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const DecodeScratch& ws, int grid, bool after_prefill,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const CacheWrite* write) {
   if (a.num_reqs == 0) return cudaSuccess;
   if (a.num_reqs > kDecodeMaxReqs || a.num_kv_heads > 8) return cudaErrorNotSupported;
   DecodeParams prm;
@@ -541,6 +592,15 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const
   prm.part_ml = ws.part_ml;
   prm.err = a.err;
   prm.wait_before_loads = after_prefill ? 0 : 1;
+  prm.k_new = write ? static_cast<const __nv_bfloat16*>(write->key) : nullptr;
+  prm.v_new = write ? static_cast<const __nv_bfloat16*>(write->value) : nullptr;
+  prm.k_new_stride = write ? write->key_stride : 0;
+  prm.v_new_stride = write ? write->value_stride : 0;
+  prm.slot_mapping = write ? write->slot_mapping : nullptr;
+  prm.key_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.key_cache));
+  prm.value_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.value_cache));
+  prm.num_slots = a.num_blocks * a.block_size;
+  if (write && after_prefill) return cudaErrorInvalidValue;  // the write must precede a prefill
   prm.stage_bytes = 2u * a.num_kv_heads * (a.head_dim / 64) * 2048u;
   const size_t fixed = 1024 + 16 * kDecodeMaxStages + 4 * (a.num_reqs + 1) + 4 * 32 + 64;
   int stages = static_cast<int>((kSmemBudget - fixed) / prm.stage_bytes);

@@ -105,10 +105,23 @@ cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, void* dst_k
 // Grid size (CTAs) of the persistent split-KV decode kernel on this device.
 int decode_grid_size(int device);
 
+// This step's new K/V rows for a cache write fused into the decode kernel
+// (strides in elements).
+struct CacheWrite {
+  const void* key;
+  const void* value;
+  int64_t key_stride;
+  int64_t value_stride;
+  const int64_t* slot_mapping;
+};
+
 // Split-KV decode of every request with query length 1 (bf16, mma + TMA).
+// With `write` set, the kernel also does reshape_and_cache of each decode
+// token (its row goes to slot_mapping[token] and is used in place of the
+// cache's copy of that position).
 cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const DecodeScratch& ws, int grid, bool after_prefill,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const CacheWrite* write = nullptr);
 
 // Chunked-prefill attention (bf16, tcgen05 + TMA + TMEM) of every request
 // with query length > 1; qmap is the [T, H, D] query as a (D, H, T) tensor map
