@@ -218,17 +218,24 @@ def reshape_and_cache_paged_attention(key, value, slot_mapping, q, key_cache, va
 # ---------------------------------------------------------------------------
 # host entry points (numpy arrays)
 # ---------------------------------------------------------------------------
-def _ptr(a: np.ndarray):
-    return a.ctypes.data_as(C.c_void_p)
+def _ptr(a: np.ndarray) -> int:
+    # the address as an int (ctypes passes it as void*); cheaper than data_as
+    return a.ctypes.data
 
 
 def build_slot_mapping(block_table: np.ndarray, query_start_loc, num_computed_tokens,
-                       block_size: int) -> np.ndarray:
+                       block_size: int, out: np.ndarray | None = None) -> np.ndarray:
+    """slot_mapping (int64 [num_tokens]) of the step, built on the host; `out`,
+    if given, is a C-contiguous int64 array of num_tokens entries (for instance
+    a view of a pinned staging buffer) written in place."""
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
     qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
     nc = np.ascontiguousarray(num_computed_tokens, dtype=np.int32)
     n = int(qsl[-1]) if len(qsl) else 0
-    out = np.empty(n, dtype=np.int64)
+    if out is None:
+        out = np.empty(n, dtype=np.int64)
+    elif out.dtype != np.int64 or out.shape != (n,) or not out.flags.c_contiguous:
+        raise ValueError(f"out must be a contiguous int64 array of {n} entries")
     _check(lib().pkv_build_slot_mapping(_ptr(bt), bt.shape[1], _ptr(qsl), _ptr(nc), len(nc),
                                         block_size, _ptr(out), n), "build_slot_mapping")
     return out
