@@ -29,6 +29,26 @@ cudaError_t raise_smem_limit_once(size_t bytes) {
   return status[dev];
 }
 
+// Launches `kern` as a programmatic dependent of the kernel before it on
+// `stream`: its blocks may become resident while that kernel finishes.  The
+// kernel must execute griddepcontrol.wait before touching memory the kernel
+// before it may read or write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Everything an attention kernel needs about one paged_attention_varlen call.
 struct AttnArgs {
   const void* q;

@@ -26,8 +26,14 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     int64_t value_stride_v, uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
     const int64_t* __restrict__ slot_mapping, int64_t num_tokens, int64_t num_slots,
     int32_t vec_per_row, uint32_t* __restrict__ err) {
-  // an attention kernel launched as this one's programmatic dependent may
-  // start its prologue now; it waits for this grid before reading the caches
+  // This grid is itself a programmatic dependent of the kernel before it,
+  // which may still read the cache or write the new rows: wait for it before
+  // any load or store.
+  grid_dependency_wait();
+  // An attention kernel launched as this one's programmatic dependent may
+  // start its prologue now (it waits for this grid before reading the
+  // caches).  Released only after the wait above, so that prologue reads
+  // metadata that work before this grid wrote.
   if (threadIdx.x == 0) grid_launch_dependents();
   // One warp per token.  The slot and up to four 16-byte chunks of the K row
   // and of the V row per lane are loaded together, so a token costs one
@@ -81,11 +87,12 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
   const int64_t blocks = (num_tokens + 7) / 8;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident blocks per SM
   const int64_t grid = blocks < cap ? blocks : cap;
-  reshape_and_cache_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), key_stride_b / 16,
-      value_stride_b / 16, static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
-      slot_mapping, num_tokens, num_slots, vpr, err);
-  return cudaGetLastError();
+  return launch_programmatic(reshape_and_cache_kernel, dim3(static_cast<unsigned>(grid)),
+                             dim3(kThreads), 0, stream, static_cast<const uint4*>(key),
+                             static_cast<const uint4*>(value), key_stride_b / 16,
+                             value_stride_b / 16, static_cast<uint4*>(key_cache),
+                             static_cast<uint4*>(value_cache), slot_mapping, num_tokens, num_slots,
+                             vpr, err);
 }
 
 }  // namespace pkv

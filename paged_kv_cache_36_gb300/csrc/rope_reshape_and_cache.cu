@@ -213,9 +213,14 @@ __device__ __forceinline__ void rope_rows(const uint4* src, uint4* dst0, uint4* 
 
 template <typename T, bool kNeox>
 __global__ void __launch_bounds__(256) rope_cache_warp_kernel(const RopeParams p) {
-  // an attention kernel launched as this one's programmatic dependent may
-  // start its prologue now; it waits for this grid before reading Q or the
-  // caches
+  // This grid is itself a programmatic dependent of the kernel before it
+  // (which may still read the cache or Q, or write the new rows): wait for
+  // it before any load or store.
+  grid_dependency_wait();
+  // An attention kernel launched as this one's programmatic dependent may
+  // start its prologue now (it waits for this grid before reading Q or the
+  // caches).  Released only after the wait above, so that prologue reads
+  // metadata that work before this grid wrote.
   if (threadIdx.x == 0) grid_launch_dependents();
   // One warp per token.  The V row's loads go out together with the position
   // and slot loads, and the K row's right after; the position's validity is
@@ -285,8 +290,8 @@ cudaError_t launch_warp_t(RopeParams p, cudaStream_t stream) {
   const int64_t blocks = (p.num_tokens + 7) / 8;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // tokens beyond this loop in the warps
   const int64_t grid = blocks < cap ? blocks : cap;
-  rope_cache_warp_kernel<T, kNeox><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_programmatic(rope_cache_warp_kernel<T, kNeox>, dim3(static_cast<unsigned>(grid)),
+                             dim3(kThreads), 0, stream, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -361,9 +366,14 @@ __device__ __forceinline__ void rotate_stage(uint8_t* st, const RopeParams& p, c
 template <typename T, bool kNeox>
 __global__ void __launch_bounds__(kStagedThreads)
     rope_cache_staged_kernel(const RopeParams p, const StageLayout L) {
-  // an attention kernel launched as this one's programmatic dependent may
-  // start its prologue now; it waits for this grid before reading Q or the
-  // caches
+  // This grid is itself a programmatic dependent of the kernel before it
+  // (which may still read the cache or Q, or write the new rows): wait for
+  // it before any load or store.
+  grid_dependency_wait();
+  // An attention kernel launched as this one's programmatic dependent may
+  // start its prologue now (it waits for this grid before reading Q or the
+  // caches).  Released only after the wait above, so that prologue reads
+  // metadata that work before this grid wrote.
   if (threadIdx.x == 0) grid_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = L.stages;
@@ -526,8 +536,8 @@ cudaError_t launch_t(const RopeParams& p, cudaStream_t stream) {
   }();
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   const int64_t grid = p.num_tokens < cap ? p.num_tokens : cap;
-  kern<<<static_cast<unsigned>(grid), kStagedThreads, smem, stream>>>(p, L);
-  return cudaGetLastError();
+  return launch_programmatic(kern, dim3(static_cast<unsigned>(grid)), dim3(kStagedThreads), smem,
+                             stream, p, L);
 }
 
 }  // namespace
