@@ -283,16 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 3) {
-    // This grid is a programmatic dependent of the kernel before it, so the
-    // set-up and plan above (metadata only) overlap that kernel's tail.  Q
-    // and the caches may be written by it (the cache write, with RoPE also
-    // Q), so the copies start only after it has completed.  Every thread
-    // that writes global memory does so after data these copies brought.
-    grid_dependency_wait();
-    // Let the decode kernel of this call be scheduled only now: it reads the
-    // caches and Q without waiting for this grid, which is safe once the
-    // cache write before this grid is known to be complete.
-    if (warp == 0 && lane == 0) grid_launch_dependents();
     // ============================ TMA producers ============================
     // warp 0 streams Q and K, warp 3 streams V.  They are separate warps so
     // that neither waits on the other's ring: two lanes of one warp would run
@@ -308,27 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = smem + (is_k ? L::kK : L::kV);
     uint32_t q_uses = 0, count = 0;
     bool ok = true;
+    bool grid_waited = false;
     for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0 && ok;
          ct = cluster_tile(++it, cid, ncl, total)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
       const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
       const int nblk = (t.nkeys + 15) / 16;
-      if (is_k) {
-        if (lane == 0) {
-          if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag)) {
-            ok = false;
-          } else {
-            mbar_arrive_expect_tx(&bars[kQFull], L::kHalf);
-            for (int dh = 0; dh < NDH; ++dh)
-              tma_load_3d(smem + L::kQ + dh * kRegion, &qmap, dh * 64, t.h * G,
-                          static_cast<int32_t>(t.qs + t.u0), &bars[kQFull]);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        ++q_uses;
-      }
       // Block ids [batch, batch + 32) in `cur`, the next 32 in flight in `nxt`.
       // A batch is checked when it becomes current, by which time its loads
       // have long completed, so no key tile waits on a block-table read.
@@ -346,6 +322,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int batch = 0;
       int32_t cur = load_ids(0), nxt = load_ids(32);
+      // This grid is a programmatic dependent of the kernel before it, so the
+      // set-up and plan above (metadata only) and the first block-table reads
+      // overlap that kernel's tail.  Q and the caches may be written by it
+      // (the cache write, with RoPE also Q), so the copies start only after
+      // it has completed.  Every thread that writes global memory does so
+      // after data these copies brought.  The decode kernel of this call is
+      // released only now: it reads the caches and Q without waiting for
+      // this grid, which is safe once the cache write before it is complete.
+      if (!grid_waited) {
+        grid_dependency_wait();
+        if (is_k && lane == 0) grid_launch_dependents();
+        grid_waited = true;
+      }
+      if (is_k) {
+        if (lane == 0) {
+          if (q_uses > 0 && !mbar_wait_or_abort(&bars[kQEmpty], (q_uses - 1) & 1, p.err, abort_flag)) {
+            ok = false;
+          } else {
+            mbar_arrive_expect_tx(&bars[kQFull], L::kHalf);
+            for (int dh = 0; dh < NDH; ++dh)
+              tma_load_3d(smem + L::kQ + dh * kRegion, &qmap, dh * 64, t.h * G,
+                          static_cast<int32_t>(t.qs + t.u0), &bars[kQFull]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++q_uses;
+      }
       cur = check_ids(cur, 0);
       cluster_wait_once();
       for (int j = 0; j < t.nkt && ok; ++j) {
@@ -384,6 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         ++count;
       }
+    }
+    if (!grid_waited) {  // a CTA without tiles releases the decode kernel the same way
+      grid_dependency_wait();
+      if (is_k && lane == 0) grid_launch_dependents();
     }
     cluster_wait_once();
     // drain: every copy into this CTA's ring (and, in a cluster, every
