@@ -66,10 +66,19 @@ def _stream_ptr(stream) -> int | None:
 
 
 def _token_stride(t) -> int:
-    # [tokens, heads, dim] with heads and dim contiguous
-    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+    # [tokens, heads, dim] with heads and dim contiguous (one stride() call:
+    # per-dimension stride(i) calls cost several times more host time)
+    st = t.stride()
+    if len(st) != 3 or st[2] != 1 or st[1] != t.shape[2]:
         raise ValueError("expected [tokens, heads, head_dim] with contiguous heads and dims")
-    return t.stride(0)
+    return st[0]
+
+
+def _row_stride(block_table) -> int:
+    st = block_table.stride()
+    if len(st) != 2 or st[1] != 1:
+        raise ValueError("block_table must be [R, max_blocks] with unit inner stride")
+    return st[0]
 
 
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, error_word=None,
@@ -170,14 +179,12 @@ def paged_attention_varlen(q, key_cache, value_cache, block_table, query_start_l
         out = torch.empty_like(q)
     if workspace is None:
         workspace = new_workspace(R, H, D, q.device)
-    if block_table.dim() != 2 or block_table.stride(1) != 1:
-        raise ValueError("block_table must be [R, max_blocks] with unit inner stride")
     code = lib().pkv_paged_attention_varlen(
         q.data_ptr(), _token_stride(q), key_cache.data_ptr(), value_cache.data_ptr(),
-        block_table.data_ptr(), block_table.stride(0), query_start_loc.data_ptr(),
+        block_table.data_ptr(), _row_stride(block_table), query_start_loc.data_ptr(),
         seq_lens.data_ptr(), num_computed_tokens.data_ptr(), float(scale), out.data_ptr(),
         _token_stride(out), T, R, nb, bs, H, hkv, D, _dtype_code(q), int(max_query_len),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+        workspace.data_ptr(), workspace.nbytes, _stream_ptr(stream))
     _check(code, "paged_attention_varlen")
     return out
 
@@ -197,8 +204,6 @@ def reshape_and_cache_paged_attention(key, value, slot_mapping, q, key_cache, va
         out = torch.empty_like(q)
     if workspace is None:
         workspace = new_workspace(R, H, D, q.device)
-    if block_table.dim() != 2 or block_table.stride(1) != 1:
-        raise ValueError("block_table must be [R, max_blocks] with unit inner stride")
     if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
         raise ValueError("caches must be contiguous")
     if slot_mapping.dtype != torch.int64:
@@ -206,11 +211,10 @@ def reshape_and_cache_paged_attention(key, value, slot_mapping, q, key_cache, va
     code = lib().pkv_reshape_and_cache_paged_attention(
         key.data_ptr(), _token_stride(key), value.data_ptr(), _token_stride(value),
         slot_mapping.data_ptr(), q.data_ptr(), _token_stride(q), key_cache.data_ptr(),
-        value_cache.data_ptr(), block_table.data_ptr(), block_table.stride(0),
+        value_cache.data_ptr(), block_table.data_ptr(), _row_stride(block_table),
         query_start_loc.data_ptr(), seq_lens.data_ptr(), num_computed_tokens.data_ptr(),
         float(scale), out.data_ptr(), _token_stride(out), T, R, nb, bs, H, hkv, D, _dtype_code(q),
-        int(max_query_len), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _stream_ptr(stream))
+        int(max_query_len), workspace.data_ptr(), workspace.nbytes, _stream_ptr(stream))
     _check(code, "reshape_and_cache_paged_attention")
     return out
 
