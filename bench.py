@@ -1119,8 +1119,9 @@ def main():
         n2 = max(20, min(args.steps // 10, 300))
         tot, _ = time_loop([mstep], n2, stream)
         mixed_ms, mixed_tokens = combine_ranks(tot / n2, float(mstep.T), dist, device)
-        # one call per placement, each a decode launch with no rows plus the
-        # prefill kernel (launched as its programmatic dependent)
+        # one call per placement: the prefill kernel alone (a call with one
+        # request of more than one token launches no decode kernel), each a
+        # programmatic dependent of the call before it
         chunk_ms = graph_time([c.attn for c in chunks] * 5)
         chunk_tflops = mstep.prefill_flops / (chunk_ms * 1e-3) / 1e12
         secondary = {
@@ -1138,8 +1139,7 @@ def main():
                 "avg_launch_ms": chunk_ms,
                 "timing": f"CUDA graph of {5 * CHUNK_COPIES} calls rotating over {CHUNK_COPIES} "
                           f"disjoint placements of the chunk in a 4096-block cache (168 MB of "
-                          f"K/V > L2); per call: the decode launch (no rows) and the prefill "
-                          f"kernel",
+                          f"K/V > L2), back to back; per call: the prefill kernel",
             },
             "decode_gbs_in_step": None,
         }

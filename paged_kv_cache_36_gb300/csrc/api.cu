@@ -416,6 +416,9 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
     e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
+  // One request with more than one token is a prefill: there is no decode
+  // row to launch for.
+  if (num_reqs == 1 && num_tokens > 1) return PKV_OK;
   e = launch_decode_bf16(a, kblk, vblk, ds, grid, prefill, st, fuse_write ? write : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
