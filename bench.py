@@ -278,7 +278,12 @@ def build_mixed_step(pkv, device):
     vf[s] = cfg.kv.value[hr].to(device)
     step = DeviceStep(pkv, kc, vc, cfg.q, torch.cat(knew), torch.cat(vnew), cfg.blocks,
                       cfg.query_len, cfg.num_computed, cfg.num_heads, device)
-    return cfg, step
+    # the same step without its prefill request (request 0): the 256 decodes alone
+    q0 = int(cfg.query_len[0])
+    decodes = DeviceStep(pkv, kc, vc, cfg.q[q0:], torch.cat(knew[1:]), torch.cat(vnew[1:]),
+                         cfg.blocks[1:], cfg.query_len[1:], cfg.num_computed[1:], cfg.num_heads,
+                         device)
+    return cfg, step, decodes
 
 
 def build_prefill_chunks(pkv, device, copies=CHUNK_COPIES, pool_blocks=4096, from_start=False):
@@ -1111,7 +1116,7 @@ def main():
     # ---- secondary: the mixed chunked-prefill step ----
     secondary = None
     if not args.no_secondary:
-        mcfg, mstep = build_mixed_step(pkv, device)
+        mcfg, mstep, mdec = build_mixed_step(pkv, device)
         chunks = build_prefill_chunks(pkv, device)
         for i in range(args.warmup):
             mstep.step()
@@ -1119,6 +1124,12 @@ def main():
         n2 = max(20, min(args.steps // 10, 300))
         tot, _ = time_loop([mstep], n2, stream)
         mixed_ms, mixed_tokens = combine_ranks(tot / n2, float(mstep.T), dist, device)
+        # the step's 256 decodes alone (their cache write and attention), to
+        # show what the prefill chunk adds to the step
+        for _ in range(args.warmup):
+            mdec.step()
+        tot_d, _ = time_loop([mdec], n2, stream)
+        decodes_only_ms = tot_d / n2
         # one call per placement: the prefill kernel alone (a call with one
         # request of more than one token launches no decode kernel), each a
         # programmatic dependent of the call before it
@@ -1141,9 +1152,11 @@ def main():
                           f"disjoint placements of the chunk in a 4096-block cache (168 MB of "
                           f"K/V > L2), back to back; per call: the prefill kernel",
             },
-            "decode_gbs_in_step": None,
+            "decodes_only_ms_per_step": decodes_only_ms,
+            "prefill_chunk_cost_in_step_ms": mixed_ms - decodes_only_ms,
+            "decodes_only_gbs": (mdec.decode_bytes + mdec.k1_bytes) / (decodes_only_ms * 1e-3) / 1e9,
         }
-        del mstep, chunks
+        del mstep, mdec, chunks
 
     extra = None
     if not args.no_secondary:
