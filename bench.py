@@ -908,6 +908,8 @@ def main():
                     help="primary timed steps only (no e2e, secondary or CPU legs), for ncu")
     ap.add_argument("--profile-prefill", action="store_true",
                     help="only --steps calls of the 512-token chunk (rotating placements), for ncu")
+    ap.add_argument("--profile-mixed", action="store_true",
+                    help="only --steps mixed chunked-prefill steps, for ncu")
     ap.add_argument("--profile-rope", action="store_true",
                     help="only --steps calls of the fused RoPE + cache write at 8192 tokens, for ncu")
     args = ap.parse_args()
@@ -959,6 +961,15 @@ def main():
         torch.cuda.synchronize()
         print(json.dumps({"profile_rope_calls": args.warmup + args.steps,
                           "error_word": int(err.item())}))
+        return
+
+    if args.profile_mixed:
+        _, mstep, _ = build_mixed_step(pkv, device)
+        for _ in range(args.warmup + args.steps):
+            mstep.step()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_mixed_steps": args.warmup + args.steps,
+                          "error_word": pkv.read_error_word(mstep.ws)}))
         return
 
     if args.profile_prefill:
