@@ -340,17 +340,19 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The cache write of this step's tokens fuses into the decode kernel when
-  // every row is a bf16 decode row; otherwise reshape_and_cache runs first.
+  // every row is a bf16 decode row; otherwise reshape_and_cache runs first,
+  // launched only once every check of the call has passed.
   const bool fuse_write = write && dtype == PKV_BF16 && max_query_len == 1;
-  if (write && !fuse_write) {
+  auto write_first = [&]() -> int {
+    if (!write || fuse_write) return PKV_OK;
     const int64_t esize = dtype == PKV_F32 ? 4 : 2;
     cudaError_t e = launch_reshape_and_cache(
         write->key, write->value, write->key_stride * esize, write->value_stride * esize,
         const_cast<void*>(key_cache), const_cast<void*>(value_cache), write->slot_mapping,
         num_tokens, num_blocks * block_size, static_cast<int64_t>(num_kv_heads) * head_dim * esize,
         reinterpret_cast<uint32_t*>(ws), st);
-    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
-  }
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "reshape_and_cache launch");
+  };
   AttnArgs a;
   a.q = q;
   a.q_stride = q_stride;
@@ -374,6 +376,8 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   a.err = reinterpret_cast<uint32_t*>(ws);
 
   if (dtype == PKV_F32) {
+    const int wrc = write_first();
+    if (wrc != PKV_OK) return wrc;
     cudaError_t e = launch_attn_rows(a, false, false, st);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "attention launch");
   }
@@ -402,6 +406,7 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   // hides behind the prefill.  In a decode-only call the decode kernel is the
   // programmatic dependent of the kernel before the call and waits for it
   // before reading Q or the caches.
+  // (Without a prefill, max_query_len is 1, so a bf16 call's write is fused.)
   const bool prefill = max_query_len != 1;
   cudaError_t e = cudaSuccess;
   if (prefill) {
@@ -412,6 +417,8 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
     rc = encode_cache_head_map(&kmap, key_cache, num_blocks, block_size, num_kv_heads, head_dim);
     if (rc != PKV_OK) return rc;
     rc = encode_cache_head_map(&vmap, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
+    if (rc != PKV_OK) return rc;
+    rc = write_first();
     if (rc != PKV_OK) return rc;
     e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
