@@ -35,25 +35,14 @@
 // issuer blocks on its own barriers, so neither waits behind the other.
 // Tiles are handed out persistently by a device-side plan over
 // query_start_loc, heaviest (most keys) first, in rows of one tile per
-// cluster that alternate direction, so clusters end close together when a
-// prompt's tiles grow from a few key tiles to many.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
+// CTA that alternate direction, so CTAs end close together when a prompt's
+// tiles grow from a few key tiles to many.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
 // an abort flag that stops all roles.
 //
-// K/V sharing across a cluster.  With a cluster of C CTAs, the members take C
-// adjacent query tiles of the same (request, KV head) and walk the same key
-// tiles in lockstep: every K/V box lands in all members' shared memory by one
-// multicast TMA load, each member issuing 1/C of each tile's boxes, and a
-// stage is refilled only after all C members' MMAs have released it (the
-// release is a multicast tcgen05.commit onto every member's empty barrier).
-// This divides the L2->SM traffic and the TMA issue work per tile by C.  A
-// member walks the key tiles of the cluster's last query row; keys beyond its
-// own rows are masked.  A member past the request's last query tile recomputes
-// that tile without storing it, so the lockstep never breaks.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "kernels.h"
 #include "pkv_device.cuh"
@@ -79,7 +68,6 @@ constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = kSBufs * kKeys;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr size_t kPrefillSmemLimit = 232448;  // 227 KiB per CTA
-constexpr int kMaxDevices = 64;
 
 enum Bar {
   kQFull, kQEmpty,
@@ -122,11 +110,10 @@ constexpr int kReqCache = 2048;
 
 struct Tile {
   int r, h, u0, ntok;
-  int nkeys;   // keys loaded for the cluster: up to its last query row's position
-  int nkt;     // key tiles walked by every member
+  int nkeys;   // keys loaded: up to the tile's last query row's position
+  int nkt;     // key tiles walked
   int64_t qs;
   int nc;
-  bool store;  // false for a member past the request's last query tile
 };
 
 template <int D>
@@ -142,11 +129,10 @@ struct Layout {
   static constexpr uint32_t kPrefix = kMisc + 16;
 };
 
-// Cluster tile `ct` -> the query tile that cluster member `rank` computes.
-// prefix[r] counts the cluster tiles of requests before r; within a request
-// cluster tiles run KV head fastest, then groups of C query tiles.
-template <int C>
-__device__ __forceinline__ Tile decode_tile(int ct, int rank, const int32_t* prefix, int R,
+// Tile `ct` -> (request, KV head, query rows).  prefix[r] counts the tiles
+// of requests before r; within a request tiles run KV head fastest, then
+// query tiles.
+__device__ __forceinline__ Tile decode_tile(int ct, const int32_t* prefix, int R,
                                             const PrefillParams& p, int tpt,
                                             const int32_t* qsl, const int32_t* num_computed) {
   int lo = 0, hi = R;  // prefix[lo] <= ct < prefix[hi]
@@ -157,29 +143,24 @@ __device__ __forceinline__ Tile decode_tile(int ct, int rank, const int32_t* pre
   Tile t;
   t.r = lo;
   const int rem = ct - prefix[lo];
-  const int grp = rem / p.hkv;
-  t.h = rem - grp * p.hkv;
+  const int qt = rem / p.hkv;
+  t.h = rem - qt * p.hkv;
   t.qs = qsl[t.r];
   const int qlen = qsl[t.r + 1] - static_cast<int>(t.qs);
   t.nc = num_computed[t.r];
-  const int nqt = (qlen + tpt - 1) / tpt;
-  const int last = min(grp * C + C, nqt) - 1;  // the cluster's last real query tile
-  int qt = grp * C + rank;
-  t.store = qt <= last;
-  if (!t.store) qt = last;
   t.u0 = qt * tpt;
   t.ntok = min(tpt, qlen - t.u0);
-  t.nkeys = t.nc + min(qlen, last * tpt + tpt);
+  t.nkeys = t.nc + t.u0 + t.ntok;
   t.nkt = (t.nkeys + kKeys - 1) / kKeys;
   return t;
 }
 
-// The it-th cluster tile of cluster cid, or -1 when there is none.  Within a
-// request later query tiles see more keys, so tiles are taken from the
-// highest index down, ncl at a time, in alternating direction: each cluster
-// starts with one of the heaviest tiles and heavy and light ones pair up.
-__device__ __forceinline__ int cluster_tile(int it, int cid, int ncl, int total) {
-  const int lin = it * ncl + ((it & 1) ? ncl - 1 - cid : cid);
+// The it-th tile of CTA cid, or -1 when there is none.  Within a request
+// later query tiles see more keys, so tiles are taken from the highest index
+// down, ncta at a time, in alternating direction: each CTA starts with one of
+// the heaviest tiles and heavy and light ones pair up.
+__device__ __forceinline__ int cta_tile(int it, int cid, int ncta, int total) {
+  const int lin = it * ncta + ((it & 1) ? ncta - 1 - cid : cid);
   return lin < total ? total - 1 - lin : -1;
 }
 
@@ -191,7 +172,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
 
 }  // namespace
 
-template <int D, int C>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                            const __grid_constant__ CUtensorMap kmap,
@@ -213,9 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = p.num_reqs;
-  const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int cid = blockIdx.x / C, ncl = gridDim.x / C;
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << C) - 1);
+  const int cid = blockIdx.x, ncta = gridDim.x;
   const int G = p.group;
   const int tpt = kRows / G;  // query tokens per tile
 
@@ -224,19 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n = 1;
       if (b >= kPFull0 && b < kPFull0 + kSBufs) n = kSoftmaxWarps;
       if (b >= kPair0 && b < kPair0 + 4) n = 2;  // the two warps sharing a quadrant
-      if ((b >= kKEmpty0 && b < kKEmpty0 + kKStages) || (b >= kVEmpty0 && b < kVEmpty0 + kVStages))
-        n = C;  // released by the MMAs of every cluster member
       mbar_init(&bars[b], n);
     }
     fence_mbar_init();
     *abort_flag = 0;
     prefix[0] = 0;
   }
-  // Cluster members' barriers must exist before any multicast copy or commit
-  // reaches them.  Every thread arrives here, after the initialisation above;
-  // each role waits only just before its first cross-CTA operation, so the
-  // members' launch skew overlaps the plan and the first local copies.
-  if (C > 1) cluster_arrive_release();
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -262,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (seq != nc + qlen || (seq + 15) / 16 > p.bt_stride) {
         if (blockIdx.x == 0) atomicOr(p.err, PKV_ERR_METADATA);
       } else {
-        nt = ((qlen + tpt - 1) / tpt + C - 1) / C * p.hkv;
+        nt = (qlen + tpt - 1) / tpt * p.hkv;
       }
     }
     prefix[r + 1] = nt;
@@ -273,13 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   block_inclusive_scan(prefix + 1, R, scan_tmp);
   __syncthreads();
   const int total = prefix[R];
-  bool cluster_waited = C == 1;  // per warp: the wait half of the barrier above
-  auto cluster_wait_once = [&]() {
-    if (!cluster_waited) {
-      cluster_wait_acquire();
-      cluster_waited = true;
-    }
-  };
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 3) {
@@ -299,10 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t q_uses = 0, count = 0;
     bool ok = true;
     bool grid_waited = false;
-    for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0 && ok;
-         ct = cluster_tile(++it, cid, ncl, total)) {
+    for (int it = 0, ct = cta_tile(0, cid, ncta, total); ct >= 0 && ok;
+         ct = cta_tile(++it, cid, ncta, total)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
+      const Tile t = decode_tile(ct, prefix, R, p, tpt, qsl_t, nc_t);
       const int32_t* row = p.block_table + static_cast<int64_t>(t.r) * p.bt_stride;
       const int nblk = (t.nkeys + 15) / 16;
       // Block ids [batch, batch + 32) in `cur`, the next 32 in flight in `nxt`.
@@ -351,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++q_uses;
       }
       cur = check_ids(cur, 0);
-      cluster_wait_once();
       for (int j = 0; j < t.nkt && ok; ++j) {
         const int b0 = j * 8;
         if (b0 >= batch + 32) {
@@ -370,19 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
           } else {
             mbar_arrive_expect_tx(&bars[full0 + st], NDH * kBox * nvalid);
-            // one box per block, landing [token half][dim half][8 keys][128 B];
-            // block k goes out from member k % C to all members
+            // one box per block, landing [token half][dim half][8 keys][128 B]
             uint8_t* dst = ring + st * L::kHalf;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              if (k < nvalid && (C == 1 || k % C == rank)) {
-                uint8_t* d = dst + k * NDH * kBox;
-                if (C == 1)
-                  tma_load_5d(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st]);
-                else
-                  tma_load_5d_multicast(d, map, 0, 0, 0, t.h, phys[k] * 2, &bars[full0 + st],
-                                        kMask);
-              }
+              if (k < nvalid)
+                tma_load_5d(dst + k * NDH * kBox, map, 0, 0, 0, t.h, phys[k] * 2,
+                            &bars[full0 + st]);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -393,21 +351,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       grid_dependency_wait();
       if (is_k && lane == 0) grid_launch_dependents();
     }
-    cluster_wait_once();
-    // drain: every copy into this CTA's ring (and, in a cluster, every
-    // member's release of it) has landed before the CTA may exit
+    // drain: every copy into this CTA's ring has landed before the CTA may
+    // exit
     if (lane == 0) {
       for (int st = 0; st < nst; ++st) {
         const uint32_t uses = count / nst + (static_cast<uint32_t>(st) < count % nst ? 1u : 0u);
         if (uses == 0) continue;
         mbar_wait(&bars[full0 + st], (uses - 1) & 1, p.err);
-        if (C > 1) mbar_wait(&bars[empty0 + st], (uses - 1) & 1, p.err);
       }
       if (is_k && q_uses > 0) mbar_wait(&bars[kQFull], (q_uses - 1) & 1, p.err);
     }
   } else if (warp == 1) {
     // ============================ QK^T issuer ============================
-    cluster_wait_once();
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
       // descriptors are built once; a stage or k-step only adds its byte
@@ -417,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + L::kK), 16, NDH * 1024);
       uint32_t q_count = 0, k_count = 0, s_count = 0;
       bool ok = true;
-      for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0 && ok && !*abort_flag;
-           ct = cluster_tile(++it, cid, ncl, total)) {
-        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
+      for (int it = 0, ct = cta_tile(0, cid, ncta, total); ct >= 0 && ok && !*abort_flag;
+           ct = cta_tile(++it, cid, ncta, total)) {
+        const Tile t = decode_tile(ct, prefix, R, p, tpt, qsl_t, nc_t);
         ok = mbar_wait_or_abort(&bars[kQFull], q_count & 1, p.err, abort_flag);
         ++q_count;
         for (int j = 0; j < t.nkt && ok; ++j) {
@@ -441,8 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_ss(d_s, q_desc + q_off, kd + k_off, idesc_s, kk > 0);
           }
           tc_commit(&bars[kSFull0 + b]);
-          if (C == 1) tc_commit(&bars[kKEmpty0 + ks]);
-          else tc_commit_multicast(&bars[kKEmpty0 + ks], kMask);
+          tc_commit(&bars[kKEmpty0 + ks]);
           if (j == t.nkt - 1) tc_commit(&bars[kQEmpty]);
           ++k_count;
           ++s_count;
@@ -451,7 +405,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ============================ PV issuer ============================
-    cluster_wait_once();
     if (lane == 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 1);
       // V stage, MN-major: the two 64-dim atoms of a group of 8 keys 1 KiB
@@ -459,9 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + L::kV), 1024, NDH * 1024);
       uint32_t v_count = 0, s_count = 0;
       bool ok = true;
-      for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0 && ok && !*abort_flag;
-           ct = cluster_tile(++it, cid, ncl, total)) {
-        const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
+      for (int it = 0, ct = cta_tile(0, cid, ncta, total); ct >= 0 && ok && !*abort_flag;
+           ct = cta_tile(++it, cid, ncta, total)) {
+        const Tile t = decode_tile(ct, prefix, R, p, tpt, qsl_t, nc_t);
         for (int j = 0; j < t.nkt && ok; ++j) {
           const int vs = v_count % kVStages;
           const int b = s_count % kSBufs;
@@ -488,15 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(&bars[kODone0 + b]);
           if (j == t.nkt - 1) tc_commit(&bars[kOFinal]);
           tc_commit(&bars[kSFree0 + b]);
-          if (C == 1) tc_commit(&bars[kVEmpty0 + vs]);
-          else tc_commit_multicast(&bars[kVEmpty0 + vs], kMask);
+          tc_commit(&bars[kVEmpty0 + vs]);
           ++v_count;
           ++s_count;
         }
       }
     }
   } else if (warp >= 4) {
-    cluster_wait_once();
     // ============================ softmax warps ============================
     // Two warps share each 32-lane quadrant of tensor memory (the same 128/4
     // rows): warp half h reads S columns [64 h, 64 h + 64).  They agree on the
@@ -521,10 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pair_uses;
       return done ? slot[(half ^ 1) * 128 + row] : mine;
     };
-    for (int it = 0, ct = cluster_tile(0, cid, ncl, total); ct >= 0;
-         ct = cluster_tile(++it, cid, ncl, total)) {
+    for (int it = 0, ct = cta_tile(0, cid, ncta, total); ct >= 0;
+         ct = cta_tile(++it, cid, ncta, total)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const Tile t = decode_tile<C>(ct, rank, prefix, R, p, tpt, qsl_t, nc_t);
+      const Tile t = decode_tile(ct, prefix, R, p, tpt, qsl_t, nc_t);
       const int u = t.u0 + row / G;  // token of this row within the request
       const bool valid_row = (row / G) < t.ntok;
       const int pos = t.nc + (valid_row ? u : t.u0 + t.ntok - 1);
@@ -607,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(s_cols, w);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_wait_st();
-        // keys past the cluster's last row were not loaded: zero their V rows
+        // keys past the tile's last row were not loaded: zero their V rows
         // so that 0 * (stale) stays 0
         if (j == t.nkt - 1 && j * kKeys + kKeys > t.nkeys) {
           // The stage's previous tile (V of key tile gs - 2) may still be in
@@ -656,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r0[32];
         tmem_ld32(lane_addr + kColO + col, r0);
         tmem_wait_ld();
-        if (valid_row && t.store) {
+        if (valid_row) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 v;
@@ -672,11 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  cluster_wait_once();  // warp 3 lanes past its role, and any other warp that skipped it
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (C > 1) cluster_sync_all();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -688,64 +637,27 @@ static size_t prefill_smem_bytes(int num_reqs, bool cache_reqs) {
          (cache_reqs ? 8 * static_cast<size_t>(num_reqs) + 4 : 0);
 }
 
-// Per device: how many clusters of an instantiation fit on the GPU at once.
-struct PrefillClusterCount {
-  std::once_flag once[kMaxDevices];
-  cudaError_t status[kMaxDevices];
-  int clusters[kMaxDevices];
-};
-
-template <int D, int C>
+template <int D>
 static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap& qmap,
                                     const CUtensorMap& kmap, const CUtensorMap& vmap, int sms,
                                     cudaStream_t stream) {
   const size_t smem = prefill_smem_bytes<D>(prm.num_reqs, prm.cache_reqs != 0);
   if (smem > kPrefillSmemLimit) return cudaErrorNotSupported;
-  auto kern = prefill_tcgen05_kernel<D, C>;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = raise_smem_limit_once<prefill_tcgen05_kernel<D>>(kPrefillSmemLimit);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  e = raise_smem_limit_once<prefill_tcgen05_kernel<D, C>>(kPrefillSmemLimit);
-  if (e != cudaSuccess) return e;
-  static PrefillClusterCount info;
-  std::call_once(info.once[dev], [&] {
-    info.clusters[dev] = sms / C;
-    info.status[dev] = cudaSuccess;
-    if (C == 1) return;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(sms / C * C));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kPrefillSmemLimit;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    info.status[dev] = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (info.status[dev] == cudaSuccess) info.clusters[dev] = n > 0 ? n : 1;
-  });
-  if (info.status[dev] != cudaSuccess) return info.status[dev];
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[1];
   // a programmatic dependent of the kernel before it in the stream (see the
   // wait at the top of the producer warps)
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(info.clusters[dev] * C));
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(sms));  // one persistent CTA per SM
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, prm);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tcgen05_kernel<D>, qmap, kmap, vmap, prm);
 }
 
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
@@ -768,21 +680,9 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, cons
   prm.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   prm.err = a.err;
   prm.cache_reqs = a.num_reqs <= kReqCache ? 1 : 0;
-  // clusters share K/V across query tiles of one request: as many members as
-  // the longest request has query tiles, up to 4
-  const int tpt = kRows / G;
-  const int qtiles = max_query_len > 0 ? (max_query_len + tpt - 1) / tpt : 4;
-  const int C = qtiles >= 4 ? 4 : qtiles >= 2 ? 2 : 1;
-  if (a.head_dim == 128) {
-    if (C == 4) return launch_prefill_t<128, 4>(prm, qmap, kmap, vmap, sms, stream);
-    if (C == 2) return launch_prefill_t<128, 2>(prm, qmap, kmap, vmap, sms, stream);
-    return launch_prefill_t<128, 1>(prm, qmap, kmap, vmap, sms, stream);
-  }
-  if (a.head_dim == 64) {
-    if (C == 4) return launch_prefill_t<64, 4>(prm, qmap, kmap, vmap, sms, stream);
-    if (C == 2) return launch_prefill_t<64, 2>(prm, qmap, kmap, vmap, sms, stream);
-    return launch_prefill_t<64, 1>(prm, qmap, kmap, vmap, sms, stream);
-  }
+  (void)max_query_len;
+  if (a.head_dim == 128) return launch_prefill_t<128>(prm, qmap, kmap, vmap, sms, stream);
+  if (a.head_dim == 64) return launch_prefill_t<64>(prm, qmap, kmap, vmap, sms, stream);
   return cudaErrorNotSupported;
 }
 

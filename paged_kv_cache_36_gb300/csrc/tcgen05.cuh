@@ -163,66 +163,3 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
 }
 
 }  // namespace pkv
-
-namespace pkv {
-
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// The two halves of a cluster barrier (every thread of every CTA of the
-// cluster executes both, in order; work may sit between them).
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Whole-CTA cluster barrier (every thread of every CTA of the cluster).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-// TMA tensor load delivered to the same shared-memory offset of every CTA in
-// `mask`, each of whose mbarrier at `bar`'s offset receives the byte count.
-__device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorMap* map, int32_t c0,
-                                                      int32_t c1, int32_t c2, uint64_t* bar,
-                                                      uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d_multicast(void* dst, const CUtensorMap* map, int32_t c0,
-                                                      int32_t c1, int32_t c2, int32_t c3,
-                                                      int32_t c4, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-// Like tc_commit, but arrives on the mbarrier at `bar`'s offset in every CTA
-// of `mask`.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-}  // namespace pkv

@@ -182,9 +182,8 @@ CASES = [
     (16, 2, 128, [1, 1, 2, 1], [513, 2, 77, 4095]),
     (64, 8, 128, [1, 1, 9], [2000, 31, 100]),
     (4, 1, 64, [1, 20, 1], [63, 16, 1000]),
-    # prefill rows spanning several query tiles, so that clusters of 2 and 4
-    # CTAs share K/V: query-tile counts that are not a multiple of the
-    # cluster size leave members past a request's last tile
+    # prefill rows spanning several query tiles, with ragged last tiles and
+    # query-tile counts that are not a multiple of 2 or 4
     (32, 8, 128, [70, 1, 45], [0, 10, 1000]),
     (32, 8, 128, [300, 129, 1, 64], [0, 2500, 40, 7]),
     (16, 4, 64, [200, 33], [5, 100]),
@@ -249,7 +248,8 @@ def test_repeated_single_tile_requests_over_long_histories():
 
 
 def test_repeated_long_chunk():
-    """The 512-token chunk at [1536, 2048) repeated: clustered K/V sharing."""
+    """The 512-token chunk at [1536, 2048) repeated: every CTA's tile plan and
+    barrier phases must give the same bits on every call."""
     _repeat_case("repeat2", [512], [1536])
 
 
