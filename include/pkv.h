@@ -624,6 +624,9 @@ int pkv_sched_finish_step(pkv_sched* s, int32_t executed_ok, int32_t* finished, 
 int pkv_sched_request(const pkv_sched* s, int32_t req_id, pkv_request_state* out);
 int pkv_sched_queues(const pkv_sched* s, int32_t* running, int32_t* num_running, int32_t* waiting,
                      int32_t* num_waiting, int32_t capacity);
+/* The SWAPPED queue (swap preemption), head first: *num ids go to
+ * out[0..capacity); PKV_E_INVALID if capacity is smaller than the queue. */
+int pkv_sched_swapped_queue(const pkv_sched* s, int32_t* out, int32_t* num, int32_t capacity);
 /* counters: [0] total preemptions, [1] recomputed tokens, [2] finished requests,
  * [3] remaining artificial failures */
 int pkv_sched_counters(const pkv_sched* s, int64_t* out4);

@@ -70,6 +70,10 @@ Readings where those sections are silent:
 * when the CPU pool cannot take a victim, the victim is preempted by
   recompute instead (the page's engine aborts; its FIXME suggests failing
   only the request; recompute keeps the request alive);
+* a victim that holds no GPU block is preempted by recompute: swap exists to
+  keep computed KV blocks, and such a victim (left RUNNING with nothing by a
+  rolled-back admission step) has none to keep and no computed token to
+  lose;
 * WAITING requests are admitted only once no request is left swapped, so
   swapped requests (older) are not overtaken;
 * a swapped request's first chunk needs its swapped blocks plus the new

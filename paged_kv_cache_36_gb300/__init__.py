@@ -490,6 +490,13 @@ class Scheduler:
                                       cap), "queues")
         return run[:nr.value].tolist(), wait[:nw.value].tolist()
 
+    def swapped_queue(self) -> list[int]:
+        cap = 1 << 16
+        buf = np.empty(cap, np.int32)
+        n = C.c_int32(0)
+        _check(lib().pkv_sched_swapped_queue(self._h, _ptr(buf), C.byref(n), cap), "swapped_queue")
+        return buf[:n.value].tolist()
+
     def counters(self) -> dict:
         out = (C.c_int64 * 4)()
         _check(lib().pkv_sched_counters(self._h, out), "counters")

@@ -113,6 +113,7 @@ SIGNATURES = {
     "pkv_sched_finish_step": (C.c_int, [vp, i32, vp, i32]),
     "pkv_sched_request": (C.c_int, [vp, i32, C.POINTER(RequestState)]),
     "pkv_sched_queues": (C.c_int, [vp, vp, vp, vp, vp, i32]),
+    "pkv_sched_swapped_queue": (C.c_int, [vp, vp, vp, i32]),
     "pkv_sched_counters": (C.c_int, [vp, P_i64]),
     "pkv_sched_allocator": (vp, [vp]),
 }

@@ -541,6 +541,16 @@ int pkv_sched_queues(const pkv_sched* s, int32_t* running, int32_t* nrun, int32_
   return PKV_OK;
 }
 
+int pkv_sched_swapped_queue(const pkv_sched* s, int32_t* out, int32_t* num, int32_t cap) {
+  PKV_NEED_S(s);
+  const auto& q = s->impl.swapped_queue();
+  if (static_cast<int64_t>(q.size()) > cap)
+    return fail(PKV_E_INVALID, "pkv_sched_swapped_queue: capacity %d too small", cap);
+  if (out) std::copy(q.begin(), q.end(), out);
+  if (num) *num = static_cast<int32_t>(q.size());
+  return PKV_OK;
+}
+
 int pkv_sched_counters(const pkv_sched* s, int64_t* out4) {
   PKV_NEED_S(s);
   if (!out4) return fail(PKV_E_INVALID, "pkv_sched_counters: null output");

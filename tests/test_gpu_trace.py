@@ -4,9 +4,11 @@ chunk size 512, max_num_seqs 256, a 16384-block pool (small enough that
 recompute preemption triggers), Llama-3-8B head shapes in bf16.
 
 Every step the C++ scheduler and the oracle scheduler are compared
-bit-exactly (plan, preemptions, admissions, block tables, slot mapping, free
-list), the step's tokens go through reshape_and_cache and paged attention on
-the GPU, and every 10th step the attention output of every request is
+bit-exactly (plan, preemptions, admissions, block tables, slot mapping), and
+so is the whole host state with the step's reservation open and again after
+its commit: free list, allocator statistics, every request's status and
+counters, the tables of every request holding blocks, and the queues.  The
+step's tokens go through reshape_and_cache and paged attention on the GPU, and every 10th step the attention output of every request is
 compared with the float64 oracle over the request's own logical K/V
 history.  K/V rows are a function of (request, position) only, so a
 recomputed request rewrites identical values.
@@ -21,6 +23,7 @@ import torch
 from oracle import attention as oa
 from oracle.scheduler import NaiveScheduler, SchedConfig
 from tests.gpu_support import compare
+from tests.host_state import assert_same_state
 from workloads import PooledRows, generate_arrivals, trace_spec
 
 pytestmark = pytest.mark.gpu
@@ -68,8 +71,7 @@ def test_trace_300_steps():
         assert slots.tolist() == rslots
         for k, row in enumerate(rrows):
             assert bt[k, :len(row)].tolist() == row
-        if step % 25 == 0:
-            assert cpp.allocator.free_list() == ref.alloc.free_list
+        assert_same_state(cpp, ref)
         T = int(qsl[-1])
         if T:
             rid_of = np.repeat([e[0] for e in pr.entries], [e[1] for e in pr.entries])
@@ -99,6 +101,7 @@ def test_trace_300_steps():
                 checked += 1
         fin_c, fin_r = cpp.finish_step(True), ref.finish_step(True)
         assert fin_c == fin_r
+        assert_same_state(cpp, ref)
         for rid in fin_r:
             hist.pop(rid, None)
     torch.cuda.synchronize()
@@ -162,6 +165,7 @@ def test_prefix_sharing_trace_300_steps():
         assert slots.tolist() == rslots
         for k, row in enumerate(rrows):
             assert bt[k, :len(row)].tolist() == row
+        assert_same_state(cpp, ref, prefix=True)
         T = int(qsl[-1])
         if T:
             rid_of = np.repeat([e[0] for e in pr.entries], [e[1] for e in pr.entries])
@@ -189,6 +193,7 @@ def test_prefix_sharing_trace_300_steps():
                 assert pkv.read_error_word(ws) == 0
                 checked += 1
         assert cpp.finish_step(True) == ref.finish_step(True)
+        assert_same_state(cpp, ref, prefix=True)
     torch.cuda.synchronize()
     assert pkv.read_error_word(ws) == 0
     st = cpp.allocator.prefix_stats()
@@ -248,6 +253,9 @@ def test_swap_preemption_trace_300_steps():
         rqsl, rseq, rnc, rrows, rslots = ref.metadata(pr)
         assert qsl.tolist() == rqsl and seq.tolist() == rseq and nc.tolist() == rnc
         assert slots.tolist() == rslots
+        for k, row in enumerate(rrows):
+            assert bt[k, :len(row)].tolist() == row
+        assert_same_state(cpp, ref, swap=True)
         T = int(qsl[-1])
         if T:
             rid_of = np.repeat([e[0] for e in pr.entries], [e[1] for e in pr.entries])
@@ -282,6 +290,7 @@ def test_swap_preemption_trace_300_steps():
                 checked += 1
         fin_c, fin_r = cpp.finish_step(True), ref.finish_step(True)
         assert fin_c == fin_r
+        assert_same_state(cpp, ref, swap=True)
         for rid in fin_r:
             hist.pop(rid, None)
     torch.cuda.synchronize()

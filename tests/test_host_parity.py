@@ -11,6 +11,7 @@ import paged_kv_cache_36_gb300 as pkv
 from oracle import paging
 from oracle.allocator import NaiveAllocator
 from oracle.scheduler import NaiveScheduler, SchedConfig
+from tests.host_state import assert_same_state
 from workloads import generate_arrivals, generate_prefix_arrivals, trace_spec
 
 
@@ -99,7 +100,10 @@ def _pair(c: SchedConfig):
     return cpp, ref
 
 
-def _compare_step(cpp, ref, arrivals_now, fail_step=False, check_tables=True):
+def _compare_step(cpp, ref, arrivals_now, fail_step=False, swap=False, prefix=False):
+    """One step of both schedulers: the plan, the step metadata, and the whole
+    host state (allocator, requests, queues) with the reservation open and
+    again after the commit or rollback."""
     for a in arrivals_now:
         if getattr(a, "tokens", ()):
             assert cpp.add_request(a.req_id, a.prompt_len, a.max_output, a.namespace, a.tokens) == \
@@ -121,13 +125,11 @@ def _compare_step(cpp, ref, arrivals_now, fail_step=False, check_tables=True):
     assert slots.tolist() == rslots
     for k, row in enumerate(rrows):
         assert bt[k, :len(row)].tolist() == row and (bt[k, len(row):] == -1).all()
-    if check_tables:
-        assert cpp.allocator.free_list() == ref.alloc.free_list
+    assert_same_state(cpp, ref, swap, prefix)
     fin_c = cpp.finish_step(not fail_step)
     fin_r = ref.finish_step(not fail_step)
     assert fin_c == fin_r
-    run, wait = cpp.queues()
-    assert run == ref.running and wait == ref.waiting
+    assert_same_state(cpp, ref, swap, prefix)
     return pc
 
 
@@ -141,13 +143,7 @@ def test_scheduler_trace_bit_exact():
     for a in generate_arrivals(spec):
         by_step.setdefault(a.step, []).append(a)
     for step in range(spec.steps):
-        _compare_step(cpp, ref, by_step.get(step, []), check_tables=(step % 10 == 0))
-        if step % 25 == 0:
-            cpp.allocator.check()
-            for rid, r in ref.reqs.items():
-                st = cpp.request(rid)
-                assert (st["num_tokens"], st["num_computed"], st["outputs"], st["preemptions"]) == \
-                    (r.num_tokens, r.num_computed, r.outputs, r.preemptions)
+        _compare_step(cpp, ref, by_step.get(step, []))
     cnt = cpp.counters()
     assert cnt["preemptions"] == ref.total_preemptions > 0
     assert cnt["recomputed_tokens"] == ref.recomputed_tokens
@@ -170,7 +166,6 @@ def test_scheduler_small_random_with_faults(seed):
                                            "max_output": rng.randint(1, 12)})())
             rid += 1
         _compare_step(cpp, ref, arrivals, fail_step=rng.random() < 0.1)
-        cpp.allocator.check()
     assert cpp.counters()["inject_left"] == ref.inject_left
 
 
@@ -255,16 +250,8 @@ def test_scheduler_prefix_trace_bit_exact():
     for a in generate_prefix_arrivals(spec):
         by_step.setdefault(a.step, []).append(a)
     for step in range(spec.steps):
-        _compare_step(cpp, ref, by_step.get(step, []), check_tables=(step % 10 == 0))
-        if step % 10 == 0:
-            p, q = cpp.allocator.prefix_stats(), ref.alloc.prefix_stats()
-            assert (p["lookups"], p["hits"], p["matched_tokens"], p["evictions"], p["indexed"],
-                    p["shared"], p["cached"]) == \
-                (q.lookups, q.hits, q.matched_tokens, q.evictions, q.indexed, q.shared,
-                 len(ref.alloc.cached))
-            assert cpp.allocator.cached_list() == ref.alloc.cached
+        _compare_step(cpp, ref, by_step.get(step, []), prefix=True)
         if step % 25 == 0:
-            cpp.allocator.check()
             ref.alloc.deep_check()
     q = ref.alloc.prefix_stats()
     assert q.hits > 100 and q.matched_tokens > 100000     # sharing actually happens
@@ -284,19 +271,37 @@ def test_scheduler_swap_mode_small_random_with_faults(seed):
                     num_cpu_blocks=rng.choice([4, 16, 200]))
     cpp, ref = _pair(c)
     rid = 0
-    swaps = 0
+    swaps = blockless_victims = 0
     for step in range(250):
         arrivals = []
         for _ in range(rng.choice([0, 0, 1, 2])):
             arrivals.append(type("A", (), {"req_id": rid, "prompt_len": rng.randint(1, 30),
                                            "max_output": rng.randint(1, 12)})())
             rid += 1
-        pc = _compare_step(cpp, ref, arrivals, fail_step=rng.random() < 0.1)
+        blockless = [r for r in ref.running if not ref.alloc.tables.get(r)]
+        pc = _compare_step(cpp, ref, arrivals, fail_step=rng.random() < 0.1, swap=True)
         swaps += len(pc["swapped_out"])
-        cpp.allocator.check()
-        assert cpp.allocator.cpu_free_list() == ref.alloc.cpu_free
+        blockless_victims += sum(1 for r in pc["preempted"] if r in blockless)
     assert swaps > 0
+    if seed == 0:
+        # victims left without blocks by a rolled-back admission step occur here
+        assert blockless_victims > 0
     assert cpp.counters()["recomputed_tokens"] == ref.recomputed_tokens
+
+
+def test_scheduler_swap_mode_blockless_victim():
+    """The swap-mode victim that holds no GPU block (left RUNNING with nothing
+    by a rolled-back admission step): both schedulers preempt it by
+    recompute, in the same step, with the same state afterwards."""
+    from tests.test_oracle_swap import _blockless_victim_scenario
+    c, reqs = _blockless_victim_scenario()
+    cpp, ref = _pair(c)
+    arrivals = [type("A", (), {"req_id": r, "prompt_len": n, "max_output": o})() for r, n, o in reqs]
+    _compare_step(cpp, ref, arrivals, fail_step=True, swap=True)
+    pc = _compare_step(cpp, ref, [], swap=True)
+    assert pc["preempted"] == [1] and pc["swapped_out"] == []
+    for _ in range(10):
+        _compare_step(cpp, ref, [], swap=True)
 
 
 def test_scheduler_trace_swap_mode_bit_exact():
@@ -312,12 +317,9 @@ def test_scheduler_trace_swap_mode_bit_exact():
         by_step.setdefault(a.step, []).append(a)
     swaps = swapins = 0
     for step in range(spec.steps):
-        pc = _compare_step(cpp, ref, by_step.get(step, []), check_tables=(step % 10 == 0))
+        pc = _compare_step(cpp, ref, by_step.get(step, []), swap=True)
         swaps += len(pc["swapped_out"])
         swapins += len(pc["swapped_in"])
-        if step % 25 == 0:
-            cpp.allocator.check()
-            assert cpp.allocator.cpu_free_list() == ref.alloc.cpu_free
     assert swaps > 10 and swapins > 10
     cnt = cpp.counters()
     assert cnt["preemptions"] == ref.total_preemptions

@@ -124,3 +124,38 @@ def test_swap_mode_resumes_without_recompute(seed):
     if c.num_cpu_blocks >= 40:
         assert s.recomputed_tokens == 0         # every preemption was a swap
     assert swapped_any and s.total_preemptions > 0
+
+
+def _blockless_victim_scenario():
+    """Two requests admitted in one step whose execution fails: the rollback
+    leaves both RUNNING with no blocks (admissions stand).  In the next step
+    one injected slot-check failure (the page's artificial-preemption hook)
+    makes the head preempt the tail of RUNNING, which holds no GPU block."""
+    c = SchedConfig(max_num_seqs=4, max_num_batched_tokens=64, chunk_size=64,
+                    max_model_len=200, block_size=4, num_blocks=8, max_blocks_per_req=50,
+                    artificial_preempt_prob=1.0, artificial_preempt_max=1,
+                    preemption_mode="swap", num_cpu_blocks=8)
+    return c, [(0, 4, 3), (1, 4, 3)]
+
+
+def test_swap_mode_victim_without_blocks_is_recomputed():
+    """A swap-mode victim that holds no GPU block has no KV cache to move to
+    the CPU pool and no computed token to lose: it is preempted by recompute
+    (back to the front of WAITING), not parked in the SWAPPED queue."""
+    c, reqs = _blockless_victim_scenario()
+    s = NaiveScheduler(c)
+    for rid, n, out in reqs:
+        assert s.add_request(rid, n, out)
+    p1 = s.step()
+    assert p1.admitted == [0, 1]
+    s.finish_step(False)                          # rollback: both hold nothing
+    assert s.running == [0, 1] and not s.alloc.tables.get(0) and not s.alloc.tables.get(1)
+    p2 = s.step()
+    assert p2.preempted == [1]
+    assert p2.swapped_out == [] and p2.swap_out_pairs == []
+    assert s.reqs[1].status == WAITING and s.waiting == [1] and s.swapped == []
+    assert s.reqs[1].num_computed == 0 and s.recomputed_tokens == 0
+    assert [e[0] for e in p2.entries] == [0]      # the head is scheduled after the preemption
+    assert s.alloc.cpu_free == list(range(8))     # nothing went to the CPU pool
+    s.finish_step(True)
+    s.alloc.check()
