@@ -48,6 +48,8 @@
 
 #include <algorithm>
 #include <cstring>
+#include <functional>
+#include <utility>
 #include <string>
 #include <vector>
 
@@ -64,11 +66,15 @@ Allocator::Allocator(int32_t num_blocks, int32_t block_size, int32_t max_blocks_
       holders_(static_cast<size_t>(num_blocks), 0), children_(static_cast<size_t>(num_blocks), 0),
       parent_(static_cast<size_t>(num_blocks), -2), key_of_(static_cast<size_t>(num_blocks)),
       lru_prev_(static_cast<size_t>(num_blocks), -1), lru_next_(static_cast<size_t>(num_blocks), -1),
-      in_cache_(static_cast<size_t>(num_blocks), 0), cpu_capacity_(num_cpu_blocks),
+      in_cache_(static_cast<size_t>(num_blocks), 0),
+      cache_seq_(static_cast<size_t>(num_blocks), 0), cpu_capacity_(num_cpu_blocks),
       cpu_ring_(static_cast<size_t>(num_cpu_blocks > 0 ? num_cpu_blocks : 0)),
       cpu_count_(num_cpu_blocks > 0 ? num_cpu_blocks : 0) {
   for (int32_t i = 0; i < num_blocks; ++i) ring_[i] = i;
   for (int32_t i = 0; i < cpu_count_; ++i) cpu_ring_[i] = i;
+  // the index holds at most one entry per block: sized once, it never
+  // rehashes in the middle of a step
+  index_.reserve(static_cast<size_t>(num_blocks));
 }
 
 int32_t Allocator::pop_front() {
@@ -108,6 +114,8 @@ void Allocator::release(int32_t b) {
 
 void Allocator::lru_push_back(int32_t b) {
   in_cache_[b] = 1;
+  cache_seq_[b] = next_seq_++;
+  if (children_[b] == 0) leaf_push(b);
   lru_prev_[b] = lru_tail_;
   lru_next_[b] = -1;
   if (lru_tail_ >= 0) lru_next_[lru_tail_] = b;
@@ -127,18 +135,42 @@ void Allocator::lru_remove(int32_t b) {
   --cached_;
 }
 
-void Allocator::evict_one() {
-  for (int32_t b = lru_head_; b >= 0; b = lru_next_[b]) {
-    if (children_[b] != 0) continue;  // not a leaf of the index
+// A cached block that no indexed block extends becomes an eviction candidate,
+// ordered by when it was released to the cache.
+void Allocator::leaf_push(int32_t b) {
+  if (leaves_.size() >= 2 * static_cast<size_t>(capacity_) + 64) {
+    // mostly stale: rebuild from the cached list (amortised over the pushes)
+    leaves_.clear();
+    for (int32_t c = lru_head_; c >= 0; c = lru_next_[c])
+      if (children_[c] == 0 && c != b) leaves_.emplace_back(cache_seq_[c], c);
+    std::make_heap(leaves_.begin(), leaves_.end(), std::greater<>());
+  }
+  leaves_.emplace_back(cache_seq_[b], b);
+  std::push_heap(leaves_.begin(), leaves_.end(), std::greater<>());
+}
+
+// Evicts the oldest-released cached block that no indexed block extends (a
+// leaf of the index): it leaves the index and goes to the back of the free
+// list.  Its parent may become a leaf in turn.  Returns false when no cached
+// block is a leaf (cannot happen while the index is consistent: the chain
+// below a cached block is cached too).
+bool Allocator::evict_one() {
+  while (!leaves_.empty()) {
+    std::pop_heap(leaves_.begin(), leaves_.end(), std::greater<>());
+    const auto [seq, b] = leaves_.back();
+    leaves_.pop_back();
+    if (!in_cache_[b] || cache_seq_[b] != seq || children_[b] != 0) continue;  // stale
     lru_remove(b);
     index_.erase(key_of_[b]);
     key_of_[b].clear();
-    if (parent_[b] >= 0) --children_[parent_[b]];
+    const int32_t parent = parent_[b];
     parent_[b] = -2;
+    if (parent >= 0 && --children_[parent] == 0 && in_cache_[parent]) leaf_push(parent);
     push_back(b);
     ++evictions_;
-    return;
+    return true;
   }
+  return false;
 }
 
 std::string Allocator::key(uint64_t ns, int32_t parent, const int32_t* tokens) const {
@@ -300,7 +332,8 @@ int Allocator::reserve(int32_t n, const int32_t* ids, const int32_t* new_tokens)
     return fail(PKV_E_NO_BLOCKS, "reserve: %lld blocks needed, %d free and %lld cached",
                 static_cast<long long>(total), count_, static_cast<long long>(cached_));
   }
-  while (count_ < total) evict_one();
+  while (count_ < total)
+    if (!evict_one()) return fail(PKV_E_STATE, "reserve: no cached block can be evicted");
   plan_.clear();
   for (int32_t i = 0; i < n; ++i) {
     ReqBlocks& r = reqs_[ids[i]];
@@ -467,7 +500,8 @@ int Allocator::swap_in(int32_t req, int32_t* pairs, int32_t cap_pairs) {
   auto it = swapped_.find(req);
   const int32_t n = static_cast<int32_t>(it->second.cpu.size());
   if (n > cap_pairs || !pairs) return fail(PKV_E_INVALID, "swap_in: pair capacity %d < %d", cap_pairs, n);
-  while (count_ < n) evict_one();
+  while (count_ < n)
+    if (!evict_one()) return fail(PKV_E_STATE, "swap_in: no cached block can be evicted");
   ReqBlocks& r = reqs_[req];
   r = ReqBlocks();
   for (int32_t k = 0; k < n; ++k) {
@@ -662,6 +696,16 @@ int Allocator::check() const {
     indexed += parent_[b] != -2;
   }
   if (indexed != static_cast<int64_t>(index_.size())) return fail(PKV_E_STATE, "index size");
+  // every cached leaf of the index has a current entry among the eviction
+  // candidates
+  std::vector<uint8_t> candidate(static_cast<size_t>(capacity_), 0);
+  for (const auto& e : leaves_)
+    if (e.second >= 0 && e.second < capacity_ && in_cache_[e.second] &&
+        cache_seq_[e.second] == e.first)
+      candidate[e.second] = 1;
+  for (int32_t b = lru_head_; b >= 0; b = lru_next_[b])
+    if (children_[b] == 0 && !candidate[b])
+      return fail(PKV_E_STATE, "cached leaf %d is not an eviction candidate", b);
   std::vector<uint8_t> cpu_seen(static_cast<size_t>(cpu_capacity_ > 0 ? cpu_capacity_ : 0), 0);
   for (int32_t i = 0; i < cpu_count_; ++i) {
     const int32_t c = cpu_ring_[(cpu_head_ + i) % cpu_capacity_];

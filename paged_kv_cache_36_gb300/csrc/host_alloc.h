@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <string>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "pkv.h"
@@ -88,7 +89,8 @@ class Allocator {
   void release(int32_t b);          // held by no request: cached if indexed, else free
   void lru_push_back(int32_t b);
   void lru_remove(int32_t b);
-  void evict_one();
+  void leaf_push(int32_t b);
+  bool evict_one();
   void index_prompt_blocks(int32_t req);
   std::string key(uint64_t ns, int32_t parent, const int32_t* tokens) const;
   int32_t lookup(uint64_t ns, int32_t parent, const int32_t* tokens) const;
@@ -110,6 +112,15 @@ class Allocator {
   std::vector<uint8_t> in_cache_;
   int32_t lru_head_ = -1, lru_tail_ = -1;
   int64_t cached_ = 0;
+  // Eviction candidates: (release sequence number, block) in a min-heap, so
+  // the oldest-released cached leaf is found without walking the cached
+  // list.  Entries go stale when their block leaves the cache, gains an
+  // indexed child or is released again (new sequence number); evict_one()
+  // drops stale entries as it meets them, and the heap is rebuilt from the
+  // cached list when stale entries outnumber live ones.
+  std::vector<uint64_t> cache_seq_;
+  uint64_t next_seq_ = 0;
+  std::vector<std::pair<uint64_t, int32_t>> leaves_;
   // prefix index: key (namespace, parent, block_size tokens) -> block
   std::unordered_map<std::string, int32_t> index_;
   int64_t lookups_ = 0, hits_ = 0, matched_tokens_ = 0, evictions_ = 0, cow_copies_ = 0;
