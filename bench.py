@@ -352,6 +352,17 @@ def graph_time(calls, reps=5):
     return statistics.median(times)
 
 
+def _rounded(obj):
+    """Floats to 6 significant digits, so that the headline line stays short."""
+    if isinstance(obj, float):
+        return float(f"{obj:.6g}")
+    if isinstance(obj, dict):
+        return {k: _rounded(v) for k, v in obj.items()}
+    if isinstance(obj, (list, tuple)):
+        return [_rounded(v) for v in obj]
+    return obj
+
+
 def combine_ranks(ms: float, units: float, dist=None, device="cpu") -> tuple[float, float]:
     """Whole-job figures of a replicas run: the slowest rank's time and the
     units (bytes or tokens) all ranks processed.  Every rank runs its own
@@ -471,6 +482,7 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         "ms_per_launch_eager": ms_eager,
         "timing": "CUDA graph of 40 launches over the 4 batches; eager: CUDA events around 40 "
                   "back-to-back binding calls",
+        "traffic": traffic_from_profile("reshape_and_cache", ["reshape_and_cache.cu"], 1.0),
     }
     # ---- the same scatter fused with RoPE of Q (32 heads) and K ----
     from workloads.generators import rope_cos_sin_table
@@ -582,6 +594,8 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         res_copy[name] = {"ms": ms, "gbs": copy_bytes / (ms * 1e-3) / 1e9}
     res_copy["device_to_device"]["frac_of_hbm_peak"] = \
         2 * copy_bytes / (res_copy["device_to_device"]["ms"] * 1e-3) / 1e9 / hbm_peak
+    res_copy["device_to_device"]["traffic"] = traffic_from_profile("copy_blocks",
+                                                                   ["copy_blocks.cu"], 1.0)
     # the link's own rate: the copy engines moving the same bytes contiguously
     dk, dv = kc[:n], vc[:n]
     link = {}
@@ -912,6 +926,12 @@ def main():
                     help="only --steps mixed chunked-prefill steps, for ncu")
     ap.add_argument("--profile-rope", action="store_true",
                     help="only --steps calls of the fused RoPE + cache write at 8192 tokens, for ncu")
+    ap.add_argument("--profile-k1", action="store_true",
+                    help="only --steps reshape_and_cache calls of 8192 tokens (4 rotating "
+                         "batches), for ncu")
+    ap.add_argument("--profile-copy", action="store_true",
+                    help="only --steps copy_blocks calls of 4096 scattered block pairs within "
+                         "a 16384-block pool, for ncu")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -961,6 +981,40 @@ def main():
         torch.cuda.synchronize()
         print(json.dumps({"profile_rope_calls": args.warmup + args.steps,
                           "error_word": int(err.item())}))
+        return
+
+    if args.profile_k1 or args.profile_copy:
+        from workloads.generators import random_block_placement
+        Hkv, D = 8, 128
+        g = torch.Generator(device=device)
+        g.manual_seed(127)
+        err = torch.zeros(1, dtype=torch.int32, device=device)
+        if args.profile_k1:
+            T = 8192
+            nbk = 4 * T // 16 + 64
+            kc = torch.empty((nbk, 16, Hkv, D), dtype=torch.bfloat16, device=device)
+            vc = torch.empty_like(kc)
+            calls = []
+            for b in random_block_placement(nbk, [T // 16] * 4, "bench", "k1 8192"):
+                b = b.astype(np.int64)
+                slots = torch.from_numpy((b[:, None] * 16 + np.arange(16)[None, :])
+                                         .reshape(-1)).to(device)
+                calls.append((torch.randn((T, Hkv, D), generator=g, device=device)
+                              .to(torch.bfloat16),
+                              torch.randn((T, Hkv, D), generator=g, device=device)
+                              .to(torch.bfloat16), kc, vc, slots))
+            for i in range(args.warmup + args.steps):
+                pkv.reshape_and_cache(*calls[i % 4], error_word=err)
+        else:
+            nbp, n = 16384, 4096
+            kc = torch.randn((nbp, 16, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+            vc = torch.randn((nbp, 16, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+            blk = random_block_placement(nbp, [2 * n], "bench", "copy blocks")[0].astype(np.int32)
+            pairs = torch.from_numpy(np.stack([blk[:n], blk[n:]], axis=1)).to(device)
+            for _ in range(args.warmup + args.steps):
+                pkv.copy_blocks(kc, vc, kc, vc, pairs, error_word=err)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_calls": args.warmup + args.steps, "error_word": int(err.item())}))
         return
 
     if args.profile_mixed:
@@ -1191,6 +1245,26 @@ def main():
 
     if rank == 0:
         clk = clocks.summary()
+        # Everything measured, in full, on a line of its own first; the
+        # headline line comes last and stays short, so that a reader of the
+        # end of the output sees all of it.
+        details = {
+            "bench_details": {
+                "roofline_decode": {"timing": "CUDA events on the launching stream around the "
+                                              "timed region's back-to-back launches (one per step)",
+                                    "peak_kind": peak_kind},
+                "e2e": {"path": "host slot_mapping build into a pinned staging buffer holding all "
+                                "of the step's inputs -> one H2D copy -> "
+                                "reshape_and_cache_paged_attention -> D2H out -> stream sync",
+                        "graph": e2e_graph},
+                "secondary": secondary,
+                "extra": extra,
+                "cpu_baseline": cpu,
+                "step_forms": forms,
+                "wall_s_timed": wall,
+            }
+        }
+        print(json.dumps(details), flush=True)
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -1198,37 +1272,34 @@ def main():
             "data": "synthetic",
             "pct_of_hbm_peak": 100.0 * value / world / hbm_peak,
             "config": {
-                "workload": "Llama-3-8B decode batch: 64 requests x 1 query, contexts U[128,4096] "
-                            "(seed 127), 32 query / 8 KV heads, head_dim 128, block_size 16, "
-                            "blocks from a 65536-block pool",
-                "num_reqs": 64, "tokens_per_step": s0.T, "bytes_per_step": step_bytes,
-                "l2": "inputs larger than L2: steps rotate over 4 disjoint placements (0.55 GB each)",
+                "workload": "Llama-3-8B decode: 64 reqs x 1 query, ctx U[128,4096], 32/8 heads, "
+                            "D 128, block 16, 65536-block pool",
+                "l2": "inputs > L2: 4 disjoint placements (0.55 GB each)",
                 "parallelism": f"replicas x{world}",
             },
-            "roofline": {"kernel": "decode_splitkv_kernel (reshape_and_cache fused)",
-                         "bound": "hbm",
+            "roofline": {"kernel": "decode_splitkv_kernel", "bound": "hbm",
                          "achieved": decode_gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": decode_gbs / hbm_peak, "peak_kind": peak_kind,
+                         "frac": decode_gbs / hbm_peak,
                          "algorithmic_bytes_per_launch": kernel_bytes,
-                         "avg_launch_ms": attn_avg_ms,
-                         "timing": "CUDA events on the launching stream around the timed "
-                                   "region's back-to-back launches (one per step)",
-                         "traffic": traffic},
+                         "avg_launch_ms": attn_avg_ms, "traffic": traffic},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "path": "host slot_mapping build into a pinned staging buffer holding all "
-                            "of the step's inputs -> one H2D copy -> "
-                            "reshape_and_cache_paged_attention -> D2H out -> stream sync",
-                    "graph": e2e_graph},
-            "secondary": secondary,
-            "extra": extra,
-            "cpu_baseline": cpu,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "cpu_baseline": None if cpu is None else {
+                "value": cpu["value"], "unit": cpu["unit"], "cores": cpu["cores"],
+                "kind": cpu["kind"], "sample": "headline batch in rotation, 12 s"},
             "gpu_launches": args.steps,
-            "step_forms": forms,
             "clocks": clk,
-            "wall_s_timed": wall,
         }
-        print(json.dumps(line), flush=True)
+        if secondary is not None:
+            pr = secondary["prefill_roofline"]
+            line["mixed_tokens_per_s_per_layer"] = {
+                "value": secondary["value"], "ms_per_step": secondary["ms_per_step"],
+                "workload": "512-token chunk + 256 decodes"}
+            line["prefill_roofline"] = {
+                "kernel": pr["kernel"], "bound": "tensor", "achieved": pr["achieved"],
+                "peak": pr["peak"], "unit": "TFLOP/s", "frac": pr["frac"],
+                "avg_launch_ms": pr["avg_launch_ms"]}
+        print(json.dumps(_rounded(line)), flush=True)
     if dist:
         dist.destroy_process_group()
 

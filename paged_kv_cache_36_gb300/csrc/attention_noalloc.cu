@@ -65,11 +65,15 @@ int scratch_address(void** out) {
   return PKV_OK;
 }
 
-// Bytes at the front of the workspace that must be zero when a call starts:
-// the 256-byte header (error word) and the int32 split counters [R * H],
-// rounded up to 256 bytes - the same layout pkv_paged_attention_varlen uses.
-size_t zeroed_prefix_bytes(int32_t num_reqs, int32_t num_heads) {
-  const size_t counters = sizeof(int32_t) * static_cast<size_t>(num_reqs) * num_heads;
+// Bytes at the front of the scratch that must be zero when a call starts.
+// pkv_paged_attention_varlen lays a workspace out for the largest batch it
+// can hold, but the two parts that must start at zero sit at the front for
+// every capacity: the 256-byte header with the error word, then the int32
+// split counters, one per (request, KV head), at r * num_kv_heads + h.  A
+// call touches only the counters of its own num_reqs requests, so clearing
+// the header and those num_reqs * num_kv_heads counters is enough.
+size_t zeroed_prefix_bytes(int32_t num_reqs, int32_t num_kv_heads) {
+  const size_t counters = sizeof(int32_t) * static_cast<size_t>(num_reqs) * num_kv_heads;
   return 256 + ((counters + 255) & ~size_t(255));
 }
 
@@ -94,7 +98,9 @@ extern "C" int pkv_paged_attention_varlen_noalloc(
   int rc = scratch_address(&scratch);
   if (rc != PKV_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(scratch, 0, zeroed_prefix_bytes(num_reqs, num_heads), st);
+  if (num_kv_heads <= 0 || num_kv_heads > num_heads)
+    return pkv::fail(PKV_E_INVALID, "pkv_paged_attention_varlen_noalloc: bad num_kv_heads");
+  cudaError_t e = cudaMemsetAsync(scratch, 0, zeroed_prefix_bytes(num_reqs, num_kv_heads), st);
   if (e != cudaSuccess)
     return pkv::fail(PKV_E_CUDA, "clearing the static scratch: %s", cudaGetErrorString(e));
   rc = pkv_paged_attention_varlen(q, q_stride, key_cache, value_cache, block_table,
