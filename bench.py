@@ -1063,7 +1063,7 @@ def main():
     # the fused kernel's algorithmic bytes: the decode reads plus the cache write
     kernel_bytes = steps[0].decode_bytes + steps[0].k1_bytes
     decode_gbs = kernel_bytes / (attn_avg_ms * 1e-3) / 1e9
-    traffic = traffic_from_profile("decode_splitkv", ["decode_splitkv.cu"], 1.0)
+    traffic = traffic_from_profile("decode_splitkv", ["decode_splitkv.cu", "decode_core.cuh"], 1.0)
     # the same steps as two calls (reshape_and_cache, then attention), as one
     # call again, and as one call with events around each launch, for comparison
     forms = None
@@ -1195,8 +1195,8 @@ def main():
             mdec.step()
         tot_d, _ = time_loop([mdec], n2, stream)
         decodes_only_ms = tot_d / n2
-        # one call per placement: the prefill kernel alone (a call with one
-        # request of more than one token launches no decode kernel), each a
+        # one call per placement: the chunk alone (a call with no decode row
+        # puts every CTA of the varlen kernel in the prefill role), each a
         # programmatic dependent of the call before it
         chunk_ms = graph_time([c.attn for c in chunks] * 5)
         chunk_tflops = mstep.prefill_flops / (chunk_ms * 1e-3) / 1e12
@@ -1209,13 +1209,13 @@ def main():
             "prefill_chunk_ms": chunk_ms,
             "prefill_tflops": chunk_tflops,
             "prefill_roofline": {
-                "kernel": "prefill_tcgen05_kernel", "bound": "tensor", "achieved": chunk_tflops,
+                "kernel": "varlen_attention_kernel", "bound": "tensor", "achieved": chunk_tflops,
                 "peak": bf16_peak, "unit": "TFLOP/s", "frac": chunk_tflops / bf16_peak,
                 "peak_kind": peak_kind, "algorithmic_flops_per_launch": mstep.prefill_flops,
                 "avg_launch_ms": chunk_ms,
                 "timing": f"CUDA graph of {5 * CHUNK_COPIES} calls rotating over {CHUNK_COPIES} "
                           f"disjoint placements of the chunk in a 4096-block cache (168 MB of "
-                          f"K/V > L2), back to back; per call: the prefill kernel",
+                          f"K/V > L2), back to back; per call: the varlen kernel, all CTAs prefill",
             },
             "decodes_only_ms_per_step": decodes_only_ms,
             "prefill_chunk_cost_in_step_ms": mixed_ms - decodes_only_ms,

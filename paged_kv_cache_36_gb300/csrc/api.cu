@@ -396,20 +396,15 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   ds.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   ds.part_o = reinterpret_cast<float*>(ws + wl.part_o);
   ds.num_slots = wl.slots;
-  // Rows with query length > 1 go to the prefill kernel, launched first as a
-  // programmatic dependent of the kernel before it: its set-up and plan read
-  // only metadata, and its copies of Q, K and V wait for that kernel (for
-  // instance reshape_and_cache) to complete.  The decode kernel follows as
-  // the prefill's programmatic dependent, released once the prefill has seen
-  // its predecessor complete; it reads nothing the prefill writes, so it is
-  // scheduled onto SMs as they free up, and with no decode rows its launch
-  // hides behind the prefill.  In a decode-only call the decode kernel is the
-  // programmatic dependent of the kernel before the call and waits for it
-  // before reading Q or the caches.
+  // A call with rows of query length > 1 runs one persistent kernel whose
+  // CTAs split between the prefill tiles and the decode rows on the device;
+  // a decode-only call runs the split-KV decode kernel.  Either is launched
+  // as a programmatic dependent of the kernel before it: its set-up and plan
+  // read only metadata, and its copies of Q, K and V wait for that kernel
+  // (for instance reshape_and_cache) to complete.
   // (Without a prefill, max_query_len is 1, so a bf16 call's write is fused.)
-  const bool prefill = max_query_len != 1;
   cudaError_t e = cudaSuccess;
-  if (prefill) {
+  if (max_query_len != 1) {
     CUtensorMap qmap, kmap, vmap;
     rc = encode_query_map(&qmap, q, q_stride, num_tokens, num_heads, num_heads / num_kv_heads,
                           head_dim);
@@ -420,13 +415,11 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
     if (rc != PKV_OK) return rc;
     rc = write_first();
     if (rc != PKV_OK) return rc;
-    e = launch_prefill_bf16(a, qmap, kmap, vmap, grid, max_query_len, st);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    e = launch_varlen_bf16(a, qmap, kmap, vmap, kblk, vblk, ds, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen attention launch");
+    return PKV_OK;
   }
-  // One request with more than one token is a prefill: there is no decode
-  // row to launch for.
-  if (num_reqs == 1 && num_tokens > 1) return PKV_OK;
-  e = launch_decode_bf16(a, kblk, vblk, ds, grid, prefill, st, fuse_write ? write : nullptr);
+  e = launch_decode_bf16(a, kblk, vblk, ds, grid, st, fuse_write ? write : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
 }

@@ -135,20 +135,25 @@ struct CacheWrite {
   const int64_t* slot_mapping;
 };
 
-// Split-KV decode of every request with query length 1 (bf16, mma + TMA).
-// With `write` set, the kernel also does reshape_and_cache of each decode
-// token (its row goes to slot_mapping[token] and is used in place of the
-// cache's copy of that position).
+// Split-KV decode of a call whose rows all have query length 1 (bf16, mma +
+// TMA), launched as a programmatic dependent of the kernel before it.  With
+// `write` set, the kernel also does reshape_and_cache of each decode token
+// (its row goes to slot_mapping[token] and is used in place of the cache's
+// copy of that position).
 cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               const DecodeScratch& ws, int grid, bool after_prefill,
-                               cudaStream_t stream, const CacheWrite* write = nullptr);
+                               const DecodeScratch& ws, int grid, cudaStream_t stream,
+                               const CacheWrite* write = nullptr);
 
-// Chunked-prefill attention (bf16, tcgen05 + TMA + TMEM) of every request
-// with query length > 1; qmap is the [T, H, D] query as a (D, H, T) tensor map
-// with a 64 x G x 128/G box.
-cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int sms, int max_query_len,
-                                cudaStream_t stream);
+// A call with rows of query length > 1 (bf16): one persistent kernel of
+// `sms` CTAs whose CTAs split between chunked-prefill attention (tcgen05 +
+// TMA + TMEM) of those rows and the split-KV decode of the rows of query
+// length 1.  qmap is the [T, H, D] query as a (D, H, T) tensor map with a
+// 64 x G x 128/G box; kmap/vmap the per-head cache maps; kblk/vblk the
+// whole-block cache maps of the decode.
+cudaError_t launch_varlen_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, const CUtensorMap& kblk,
+                               const CUtensorMap& vblk, const DecodeScratch& ws, int sms,
+                               cudaStream_t stream);
 
 // CUDA-core attention, one warp per (query row, head); fp32 path for all rows,
 // or only rows of requests with query length > 1 when skip_decode is set.

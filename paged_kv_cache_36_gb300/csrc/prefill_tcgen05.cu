@@ -39,12 +39,22 @@
 // tiles grow from a few key tiles to many.  Every wait is bounded; a timeout sets PKV_ERR_TIMEOUT and
 // an abort flag that stops all roles.
 //
+// One kernel per call.  The grid is one CTA per SM, and the call's decode
+// rows (query length 1) run in the same grid: after the plan every CTA
+// knows the step's prefill and decode work and takes the same decision
+// (mixed_split.cuh), CTAs [0, n_p) run the prefill tiles as above and CTAs
+// [n_p, S) run the split-KV decode body (decode_core.cuh) over the decode
+// rows.  The two parts of a mixed step thus overlap on disjoint SMs within
+// one launch, with no CTA waiting for another to leave its SM.
+//
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "decode_core.cuh"
 #include "kernels.h"
+#include "mixed_split.cuh"
 #include "pkv_device.cuh"
 #include "tcgen05.cuh"
 
@@ -102,6 +112,7 @@ struct PrefillParams {
   float scale_log2;
   uint32_t* err;
   int32_t cache_reqs;  // query_start_loc and num_computed copied to shared memory
+  int32_t head_dim;
 };
 
 // Batches of up to this many requests keep query_start_loc and num_computed
@@ -125,8 +136,9 @@ struct Layout {
   static constexpr uint32_t kV = kK + kKStages * kHalf;
   static constexpr uint32_t kBars = kV + kVStages * kHalf;
   static constexpr uint32_t kXch = kBars + 8 * kNumBars;      // [2 parity][2 half][128 rows] floats
-  static constexpr uint32_t kMisc = kXch + 2 * 2 * 128 * 4;   // tmem slot, abort flag
-  static constexpr uint32_t kPrefix = kMisc + 16;
+  static constexpr uint32_t kMisc = kXch + 2 * 2 * 128 * 4;   // tmem slot, abort flag, n_p
+  static constexpr uint32_t kWork = kMisc + 16;                // one MixedWork per warp
+  static constexpr uint32_t kPrefix = kWork + 32 * (kThreads / 32);
 };
 
 // Tile `ct` -> (request, KV head, query rows).  prefix[r] counts the tiles
@@ -172,11 +184,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
 
 }  // namespace
 
-template <int D>
+static_assert(sizeof(MixedWork) == 32, "one 32-byte slot of work sums per warp");
+
+// qmap/kmap/vmap: the prefill's query and per-head cache maps; kblk/vblk:
+// the decode's whole-block cache maps.
+template <int D, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
-                           const __grid_constant__ CUtensorMap kmap,
-                           const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    varlen_attention_kernel(const __grid_constant__ CUtensorMap qmap,
+                            const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap,
+                            const __grid_constant__ CUtensorMap kblk,
+                            const __grid_constant__ CUtensorMap vblk, const PrefillParams p,
+                            const DecodeParams dp) {
   using L = Layout<D>;
   constexpr int NDH = L::NDH;
   extern __shared__ uint8_t smem_raw[];
@@ -185,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xch = reinterpret_cast<float*>(smem + L::kXch);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int* np_slot = reinterpret_cast<int*>(smem + L::kMisc + 8);
+  MixedWork* warp_work = reinterpret_cast<MixedWork*>(smem + L::kWork);  // [warps]
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kPrefix);
   int32_t* scan_tmp = prefix + p.num_reqs + 1;
   int32_t* req_qsl = scan_tmp + 32;            // [R + 1] when cached
@@ -194,18 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = p.num_reqs;
-  const int cid = blockIdx.x, ncta = gridDim.x;
+  const int cid = blockIdx.x;
   const int G = p.group;
   const int tpt = kRows / G;  // query tokens per tile
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < kNumBars; ++b) {
-      uint32_t n = 1;
-      if (b >= kPFull0 && b < kPFull0 + kSBufs) n = kSoftmaxWarps;
-      if (b >= kPair0 && b < kPair0 + 4) n = 2;  // the two warps sharing a quadrant
-      mbar_init(&bars[b], n);
-    }
-    fence_mbar_init();
     *abort_flag = 0;
     prefix[0] = 0;
   }
@@ -219,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&vmap);
   }
   // ---- plan: tiles per prefill request (all of a request's metadata in
-  // one round of loads) ----
+  // one round of loads), and the step's prefill and decode work ----
+  MixedWork mine = {0, 0, 0, 0, 0};
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     const int q0 = __ldg(p.qsl + r), q1 = __ldg(p.qsl + r + 1);
     const int seq = __ldg(p.seq_lens + r), nc = __ldg(p.num_computed + r);
@@ -229,9 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r == R - 1) req_qsl[R] = q1;
     }
     const int qlen = q1 - q0;
+    mixed_work_add(mine, qlen, nc, seq, p.hkv, G, p.head_dim);
     int nt = 0;
     if (qlen > 1) {
-      if (seq != nc + qlen || (seq + 15) / 16 > p.bt_stride) {
+      if (nc < 0 || seq != nc + qlen || (seq + 15) / 16 > p.bt_stride) {
         if (blockIdx.x == 0) atomicOr(p.err, PKV_ERR_METADATA);
       } else {
         nt = (qlen + tpt - 1) / tpt * p.hkv;
@@ -239,13 +255,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     prefix[r + 1] = nt;
   }
+  mixed_work_warp_sum(mine);
+  if (lane == 0) warp_work[warp] = mine;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The roles: every CTA reaches the same n_p from the same sums.  Only a
+  // prefill CTA sets up the barriers of the prefill pipeline.
+  if (threadIdx.x == 0) {
+    MixedWork w = {0, 0, 0, 0, 0};
+    for (int i = 0; i < kThreads / 32; ++i) {
+      const MixedWork& x = warp_work[i];
+      w.prefill_tiles += x.prefill_tiles;
+      w.prefill_units += x.prefill_units;
+      w.decode_bytes += x.decode_bytes;
+      w.prefill_rows += x.prefill_rows;
+      w.decode_rows += x.decode_rows;
+    }
+    const int n_p = mixed_prefill_ctas(w, gridDim.x);
+    *np_slot = n_p;
+    if (cid < n_p) {
+      for (int b = 0; b < kNumBars; ++b) {
+        uint32_t n = 1;
+        if (b >= kPFull0 && b < kPFull0 + kSBufs) n = kSoftmaxWarps;
+        if (b >= kPair0 && b < kPair0 + 4) n = 2;  // the two warps sharing a quadrant
+        mbar_init(&bars[b], n);
+      }
+      fence_mbar_init();
+    }
+  }
   block_inclusive_scan(prefix + 1, R, scan_tmp);
   __syncthreads();
   const int total = prefix[R];
+  const int ncta = *np_slot;
   const uint32_t tmem = *tmem_slot;
+  if (cid >= ncta) {
+    // ---- decode role: hand back the tensor memory, then the decode body
+    // over CTAs [n_p, S) ----
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    __syncthreads();  // every thread has read the slots above; the body reuses the memory
+    decode_cta<D, NT>(kblk, vblk, dp, smem, cid - ncta, static_cast<int>(gridDim.x) - ncta);
+    return;
+  }
 
   if (warp == 0 || warp == 3) {
     // ============================ TMA producers ============================
@@ -292,9 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // overlap that kernel's tail.  Q and the caches may be written by it
       // (the cache write, with RoPE also Q), so the copies start only after
       // it has completed.  Every thread that writes global memory does so
-      // after data these copies brought.  The decode kernel of this call is
-      // released only now: it reads the caches and Q without waiting for
-      // this grid, which is safe once the cache write before it is complete.
+      // after data these copies brought.  The kernel after this one is
+      // released here (it waits for this grid to complete before it touches
+      // memory this grid uses).
       if (!grid_waited) {
         grid_dependency_wait();
         if (is_k && lane == 0) grid_launch_dependents();
@@ -347,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++count;
       }
     }
-    if (!grid_waited) {  // a CTA without tiles releases the decode kernel the same way
+    if (!grid_waited) {  // a CTA without tiles waits and releases the same way
       grid_dependency_wait();
       if (is_k && lane == 0) grid_launch_dependents();
     }
@@ -637,18 +688,18 @@ static size_t prefill_smem_bytes(int num_reqs, bool cache_reqs) {
          (cache_reqs ? 8 * static_cast<size_t>(num_reqs) + 4 : 0);
 }
 
-template <int D>
-static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap& qmap,
-                                    const CUtensorMap& kmap, const CUtensorMap& vmap, int sms,
-                                    cudaStream_t stream) {
-  const size_t smem = prefill_smem_bytes<D>(prm.num_reqs, prm.cache_reqs != 0);
-  if (smem > kPrefillSmemLimit) return cudaErrorNotSupported;
-  cudaError_t e = raise_smem_limit_once<prefill_tcgen05_kernel<D>>(kPrefillSmemLimit);
+template <int D, int NT>
+static cudaError_t launch_varlen_t(const PrefillParams& prm, const DecodeParams& dp,
+                                   size_t smem, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, const CUtensorMap& kblk,
+                                   const CUtensorMap& vblk, int sms, cudaStream_t stream) {
+  auto kern = varlen_attention_kernel<D, NT>;
+  cudaError_t e = raise_smem_limit_once<varlen_attention_kernel<D, NT>>(kPrefillSmemLimit);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   // a programmatic dependent of the kernel before it in the stream (see the
-  // wait at the top of the producer warps)
+  // waits in the producer warps of both roles)
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(sms));  // one persistent CTA per SM
@@ -657,14 +708,16 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap&
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tcgen05_kernel<D>, qmap, kmap, vmap, prm);
+  return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, kblk, vblk, prm, dp);
 }
 
-cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int sms, int max_query_len,
-                                cudaStream_t stream) {
+cudaError_t launch_varlen_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, const CUtensorMap& kblk,
+                               const CUtensorMap& vblk, const DecodeScratch& ws, int sms,
+                               cudaStream_t stream) {
   const int G = a.num_heads / a.num_kv_heads;
   if (G > 128 || kRows % G) return cudaErrorNotSupported;
+  if (sms < 2) return cudaErrorNotSupported;  // each role keeps a CTA
   PrefillParams prm;
   prm.block_table = a.block_table;
   prm.bt_stride = a.bt_stride;
@@ -680,9 +733,28 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, const CUtensorMap& qmap, cons
   prm.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   prm.err = a.err;
   prm.cache_reqs = a.num_reqs <= kReqCache ? 1 : 0;
-  (void)max_query_len;
-  if (a.head_dim == 128) return launch_prefill_t<128>(prm, qmap, kmap, vmap, sms, stream);
-  if (a.head_dim == 64) return launch_prefill_t<64>(prm, qmap, kmap, vmap, sms, stream);
+  prm.head_dim = a.head_dim;
+  // The decode role follows the same kernel before this one as the prefill
+  // role (for instance the cache write), so it waits for it too.
+  DecodeParams dp;
+  size_t dsmem = 0;
+  cudaError_t e = make_decode_params(a, ws, true, nullptr, kPrefillSmemLimit, &dp, &dsmem);
+  if (e != cudaSuccess) return e;
+  const bool wide = G > 8;
+  if (a.head_dim == 128) {
+    size_t smem = prefill_smem_bytes<128>(prm.num_reqs, prm.cache_reqs != 0);
+    if (smem < dsmem) smem = dsmem;
+    if (smem > kPrefillSmemLimit) return cudaErrorNotSupported;
+    return wide ? launch_varlen_t<128, 2>(prm, dp, smem, qmap, kmap, vmap, kblk, vblk, sms, stream)
+                : launch_varlen_t<128, 1>(prm, dp, smem, qmap, kmap, vmap, kblk, vblk, sms, stream);
+  }
+  if (a.head_dim == 64) {
+    size_t smem = prefill_smem_bytes<64>(prm.num_reqs, prm.cache_reqs != 0);
+    if (smem < dsmem) smem = dsmem;
+    if (smem > kPrefillSmemLimit) return cudaErrorNotSupported;
+    return wide ? launch_varlen_t<64, 2>(prm, dp, smem, qmap, kmap, vmap, kblk, vblk, sms, stream)
+                : launch_varlen_t<64, 1>(prm, dp, smem, qmap, kmap, vmap, kblk, vblk, sms, stream);
+  }
   return cudaErrorNotSupported;
 }
 
