@@ -283,6 +283,9 @@ def build_mixed_step(pkv, device):
     decodes = DeviceStep(pkv, kc, vc, cfg.q[q0:], torch.cat(knew[1:]), torch.cat(vnew[1:]),
                          cfg.blocks[1:], cfg.query_len[1:], cfg.num_computed[1:], cfg.num_heads,
                          device)
+    # each step is one call of the fused entry: the cache write and the
+    # attention in one kernel
+    step.fuse = decodes.fuse = True
     return cfg, step, decodes
 
 

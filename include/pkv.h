@@ -104,15 +104,19 @@ int pkv_reshape_and_cache(const void* key, const void* value, int64_t key_stride
  * token strides key_stride / value_stride (elements, 16-byte multiples);
  * slot_mapping: device int64 [num_tokens]; every other argument as for
  * pkv_paged_attention_varlen.
- * When dtype is PKV_BF16 and max_query_len is 1 (a decode-only step) the two
- * run as ONE kernel: the CTA that reads a request's last block writes that
- * token's K and V rows to slot_mapping[token] and uses them in place of the
- * cache's copy, so the step costs one launch and no read-after-write through
- * memory.  This requires slot_mapping[token] to be the block table's slot of
- * position seq_len - 1 (what pkv_build_slot_mapping produces); a token whose
- * slot differs still has its rows written at slot_mapping[token], and
- * PKV_ERR_METADATA is set.  Otherwise reshape_and_cache runs as its own
- * kernel first.
+ * When dtype is PKV_BF16 the two run as ONE kernel, so the step costs one
+ * launch.  For a decode row (query length 1) the CTA that reads the
+ * request's last block writes that token's K and V rows to
+ * slot_mapping[token] and uses them in place of the cache's copy (no
+ * read-after-write through memory).  For a row of query length > 1 each
+ * prefill CTA writes the rows of its own query tiles, and the prefill CTAs
+ * meet at a counter in the workspace header before any of them reads K or
+ * V.  slot_mapping[token] must be the block table's slot of the token's
+ * position (what pkv_build_slot_mapping produces): a token whose slot
+ * differs still has its rows written at slot_mapping[token], and
+ * PKV_ERR_METADATA is set.  Rows of a request whose metadata fails the
+ * attention's checks (PKV_ERR_METADATA) are not written.  For PKV_F32
+ * reshape_and_cache runs as its own kernel first.
  * ---------------------------------------------------------------------- */
 int pkv_reshape_and_cache_paged_attention(
     const void* key, int64_t key_stride, const void* value, int64_t value_stride,

@@ -15,7 +15,8 @@ namespace pkv {
 namespace {
 
 constexpr int kVersion = 1;
-constexpr size_t kHeaderBytes = 256;  // error word + padding
+// error word, the prefill CTAs' two meeting counters, padding
+constexpr size_t kHeaderBytes = 256;
 constexpr int64_t kMaxTmaRows = 0x7fffffffLL;
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -339,10 +340,10 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The cache write of this step's tokens fuses into the decode kernel when
-  // every row is a bf16 decode row; otherwise reshape_and_cache runs first,
-  // launched only once every check of the call has passed.
-  const bool fuse_write = write && dtype == PKV_BF16 && max_query_len == 1;
+  // The cache write of this step's tokens fuses into the bf16 attention
+  // kernel; for fp32 reshape_and_cache runs first, launched only once every
+  // check of the call has passed.
+  const bool fuse_write = write && dtype == PKV_BF16;
   auto write_first = [&]() -> int {
     if (!write || fuse_write) return PKV_OK;
     const int64_t esize = dtype == PKV_F32 ? 4 : 2;
@@ -402,7 +403,6 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
   // as a programmatic dependent of the kernel before it: its set-up and plan
   // read only metadata, and its copies of Q, K and V wait for that kernel
   // (for instance reshape_and_cache) to complete.
-  // (Without a prefill, max_query_len is 1, so a bf16 call's write is fused.)
   cudaError_t e = cudaSuccess;
   if (max_query_len != 1) {
     CUtensorMap qmap, kmap, vmap;
@@ -413,9 +413,8 @@ static int paged_attention_launch(const void* q, int64_t q_stride, const void* k
     if (rc != PKV_OK) return rc;
     rc = encode_cache_head_map(&vmap, value_cache, num_blocks, block_size, num_kv_heads, head_dim);
     if (rc != PKV_OK) return rc;
-    rc = write_first();
-    if (rc != PKV_OK) return rc;
-    e = launch_varlen_bf16(a, qmap, kmap, vmap, kblk, vblk, ds, grid, st);
+    e = launch_varlen_bf16(a, qmap, kmap, vmap, kblk, vblk, ds, grid, st,
+                           fuse_write ? write : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "varlen attention launch");
     return PKV_OK;
   }

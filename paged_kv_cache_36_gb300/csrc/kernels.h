@@ -149,11 +149,14 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const
 // TMA + TMEM) of those rows and the split-KV decode of the rows of query
 // length 1.  qmap is the [T, H, D] query as a (D, H, T) tensor map with a
 // 64 x G x 128/G box; kmap/vmap the per-head cache maps; kblk/vblk the
-// whole-block cache maps of the decode.
+// whole-block cache maps of the decode.  With `write` set the kernel also
+// does the call's reshape_and_cache (every row's new K/V to its slot) before
+// attending; words 1 and 2 of the workspace header (after the error word)
+// are then the prefill CTAs' meeting counter.
 cudaError_t launch_varlen_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, const CUtensorMap& kblk,
                                const CUtensorMap& vblk, const DecodeScratch& ws, int sms,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const CacheWrite* write = nullptr);
 
 // CUDA-core attention, one warp per (query row, head); fp32 path for all rows,
 // or only rows of requests with query length > 1 when skip_decode is set.

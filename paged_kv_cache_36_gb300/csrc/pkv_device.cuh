@@ -154,6 +154,43 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy global-memory writes before later
+// async-proxy (TMA) reads of the same memory, by this or another thread.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One thread of each of n co-resident CTAs calls this; it returns once all n
+// have arrived, with their earlier global writes visible.  bar[0] counts
+// arrivals and bar[1] departures; the last CTA to leave sets both back to
+// zero, so the words are ready for the next grid.  Gives up after
+// kWaitLimitCycles (PKV_ERR_TIMEOUT, returns false).
+__device__ __forceinline__ bool cta_group_barrier(uint32_t* bar, uint32_t n, uint32_t* err) {
+  __threadfence();
+  atomicAdd(bar, 1u);
+  bool ok = true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(bar) < n) {
+    if (clock64() - t0 > kWaitLimitCycles) {
+      atomicOr(err, PKV_ERR_TIMEOUT);
+      ok = false;
+      break;
+    }
+    __nanosleep(64);
+  }
+  if (atomicAdd(bar + 1, 1u) == n - 1) {
+    atomicExch(bar, 0u);
+    atomicExch(bar + 1, 0u);
+  }
+  return ok;
+}
+
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {

@@ -113,6 +113,17 @@ struct PrefillParams {
   uint32_t* err;
   int32_t cache_reqs;  // query_start_loc and num_computed copied to shared memory
   int32_t head_dim;
+  // Fused reshape_and_cache of the prefill rows' tokens (k_new == nullptr:
+  // off): row t of k_new / v_new goes to slot_mapping[t] of the caches.
+  const uint4* k_new;
+  const uint4* v_new;
+  int64_t k_new_stride;  // 16-byte vectors per token
+  int64_t v_new_stride;
+  const int64_t* slot_mapping;
+  uint4* key_cache;
+  uint4* value_cache;
+  int64_t num_slots;
+  uint32_t* barrier;     // two zeroed words shared by the prefill CTAs
 };
 
 // Batches of up to this many requests keep query_start_loc and num_computed
@@ -174,6 +185,61 @@ __device__ __forceinline__ Tile decode_tile(int ct, const int32_t* prefix, int R
 __device__ __forceinline__ int cta_tile(int it, int cid, int ncta, int total) {
   const int lin = it * ncta + ((it & 1) ? ncta - 1 - cid : cid);
   return lin < total ? total - 1 - lin : -1;
+}
+
+// The fused cache write of one tile's tokens and KV head: K and V rows of
+// tokens [u0, u0 + ntok) of request r, head h, to their slots.  Every (token,
+// KV head) of a prefill row belongs to exactly one tile, so the tiles of all
+// prefill CTAs write each row once.  The slot must be the one the block table
+// gives for the token's position (else PKV_ERR_METADATA); slot < 0 is
+// padding and a slot past the pool is skipped with PKV_ERR_SLOT.
+template <int D>
+__device__ __forceinline__ void write_tile_rows(const PrefillParams& p, const Tile& t) {
+  constexpr int kVec = D / 8;  // 16-byte vectors in one head's row
+  const int n = t.ntok * 2 * kVec;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int u = i / (2 * kVec);
+    const int rem = i - u * 2 * kVec;
+    const bool is_v = rem >= kVec;
+    const int c = is_v ? rem - kVec : rem;
+    const int64_t tok = t.qs + t.u0 + u;
+    const int64_t slot = __ldg(p.slot_mapping + tok);
+    const int pos = t.nc + t.u0 + u;
+    if (c == 0 && !is_v) {
+      const int64_t want =
+          static_cast<int64_t>(__ldg(p.block_table + static_cast<int64_t>(t.r) * p.bt_stride + pos / 16)) *
+              16 + pos % 16;
+      if (slot != want) atomicOr(p.err, PKV_ERR_METADATA);
+      if (slot >= p.num_slots) atomicOr(p.err, PKV_ERR_SLOT);
+    }
+    if (slot < 0 || slot >= p.num_slots) continue;
+    const uint4 v = __ldg((is_v ? p.v_new + tok * p.v_new_stride : p.k_new + tok * p.k_new_stride) +
+                          t.h * kVec + c);
+    (is_v ? p.value_cache : p.key_cache)[(slot * p.hkv + t.h) * kVec + c] = v;
+  }
+}
+
+// Transposes NV x NV blocks of 16-byte values across groups of NV lanes
+// (NV a power of two <= 32): afterwards lane NV g + j holds in v[k] what lane
+// NV g + k held in v[j].  Butterfly exchanges, log2(NV) rounds of shuffles.
+template <int NV>
+__device__ __forceinline__ void transpose_lane_groups(uint4 (&v)[NV], int lane) {
+#pragma unroll
+  for (int s = 1; s < NV; s <<= 1) {
+    const bool hi = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      if (i & s) continue;
+      // pair (i, i + s): the low lane sends v[i + s], the high lane v[i]
+      const uint4 x = hi ? v[i] : v[i + s];
+      uint4 y;
+      y.x = __shfl_xor_sync(0xffffffffu, x.x, s);
+      y.y = __shfl_xor_sync(0xffffffffu, x.y, s);
+      y.z = __shfl_xor_sync(0xffffffffu, x.z, s);
+      y.w = __shfl_xor_sync(0xffffffffu, x.w, s);
+      if (hi) v[i] = y; else v[i + s] = y;
+    }
+  }
 }
 
 // All lanes of the calling warp wait; the result is made warp-uniform.
@@ -296,6 +362,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();  // every thread has read the slots above; the body reuses the memory
     decode_cta<D, NT>(kblk, vblk, dp, smem, cid - ncta, static_cast<int>(gridDim.x) - ncta);
     return;
+  }
+
+  if (p.k_new != nullptr) {
+    // ---- fused reshape_and_cache of the prefill rows ----
+    // The kernel before this one may still read the caches (or write the new
+    // rows): wait for it.  Each CTA writes the rows of its own tiles, then
+    // the prefill CTAs meet at a counter in the workspace, so that every
+    // tile's copies find every row of its keys in the cache.  The prefill
+    // CTAs are one per SM and all co-resident; the wait is bounded.
+    grid_dependency_wait();
+    for (int it = 0, ct = cta_tile(0, cid, ncta, total); ct >= 0;
+         ct = cta_tile(++it, cid, ncta, total))
+      write_tile_rows<D>(p, decode_tile(ct, prefix, R, p, tpt, qsl_t, nc_t));
+    fence_proxy_async_global();
+    __syncthreads();
+    if (threadIdx.x == 0 && !cta_group_barrier(p.barrier, ncta, p.err)) *abort_flag = 1;
+    __syncthreads();
+    fence_proxy_async_global();
   }
 
   if (warp == 0 || warp == 3) {
@@ -649,25 +733,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++tiles_done;
       tc_fence_after();
       const float inv = 1.f / (l + exchange(l));
-      __nv_bfloat16* orow =
-          p.out + (t.qs + u) * p.out_stride + static_cast<int64_t>(t.h * G + row % G) * D;
-      // this warp writes output dims [half * D/2, half * D/2 + D/2)
+      // This warp holds output dims [half * D/2, half * D/2 + D/2) of its 32
+      // rows: NV 16-byte pieces per row.  A transpose among groups of NV
+      // lanes turns that into NV rows per group with one piece each per
+      // lane, so every store instruction writes whole rows' segments
+      // (contiguous bytes) instead of 16 bytes in each of 32 rows.
+      constexpr int NV = D / 16;
+      uint4 seg[NV];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        const uint32_t col = half * (D / 2) + c * 32;
         uint32_t r0[32];
-        tmem_ld32(lane_addr + kColO + col, r0);
+        tmem_ld32(lane_addr + kColO + half * (D / 2) + c * 32, r0);
         tmem_wait_ld();
-        if (valid_row) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(r0[q4 * 8 + 0]) * inv, __uint_as_float(r0[q4 * 8 + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(r0[q4 * 8 + 2]) * inv, __uint_as_float(r0[q4 * 8 + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(r0[q4 * 8 + 4]) * inv, __uint_as_float(r0[q4 * 8 + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(r0[q4 * 8 + 6]) * inv, __uint_as_float(r0[q4 * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + col + q4 * 8) = v;
-          }
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4& v = seg[c * 4 + q4];
+          v.x = pack_bf16(__uint_as_float(r0[q4 * 8 + 0]) * inv, __uint_as_float(r0[q4 * 8 + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(r0[q4 * 8 + 2]) * inv, __uint_as_float(r0[q4 * 8 + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(r0[q4 * 8 + 4]) * inv, __uint_as_float(r0[q4 * 8 + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(r0[q4 * 8 + 6]) * inv, __uint_as_float(r0[q4 * 8 + 7]) * inv);
+        }
+      }
+      transpose_lane_groups<NV>(seg, lane);
+      // lane NV g + j now holds piece j of rows NV g + k (k < NV) of the warp
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int trow = quad * 32 + (lane & ~(NV - 1)) + k;  // tile row
+        if (trow / G < t.ntok) {
+          __nv_bfloat16* dst = p.out + (t.qs + t.u0 + trow / G) * p.out_stride +
+                               static_cast<int64_t>(t.h * G + trow % G) * D + half * (D / 2) +
+                               (lane & (NV - 1)) * 8;
+          *reinterpret_cast<uint4*>(dst) = seg[k];
         }
       }
       tc_fence_before();
@@ -714,7 +810,7 @@ static cudaError_t launch_varlen_t(const PrefillParams& prm, const DecodeParams&
 cudaError_t launch_varlen_bf16(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, const CUtensorMap& kblk,
                                const CUtensorMap& vblk, const DecodeScratch& ws, int sms,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const CacheWrite* write) {
   const int G = a.num_heads / a.num_kv_heads;
   if (G > 128 || kRows % G) return cudaErrorNotSupported;
   if (sms < 2) return cudaErrorNotSupported;  // each role keeps a CTA
@@ -734,11 +830,20 @@ cudaError_t launch_varlen_bf16(const AttnArgs& a, const CUtensorMap& qmap, const
   prm.err = a.err;
   prm.cache_reqs = a.num_reqs <= kReqCache ? 1 : 0;
   prm.head_dim = a.head_dim;
+  prm.k_new = write ? static_cast<const uint4*>(write->key) : nullptr;
+  prm.v_new = write ? static_cast<const uint4*>(write->value) : nullptr;
+  prm.k_new_stride = write ? write->key_stride / 8 : 0;  // bf16 elements -> 16-byte vectors
+  prm.v_new_stride = write ? write->value_stride / 8 : 0;
+  prm.slot_mapping = write ? write->slot_mapping : nullptr;
+  prm.key_cache = static_cast<uint4*>(const_cast<void*>(a.key_cache));
+  prm.value_cache = static_cast<uint4*>(const_cast<void*>(a.value_cache));
+  prm.num_slots = a.num_blocks * a.block_size;
+  prm.barrier = a.err + 1;  // words 1 and 2 of the workspace header
   // The decode role follows the same kernel before this one as the prefill
-  // role (for instance the cache write), so it waits for it too.
+  // role, so it waits for it too; it writes the decode rows' new K/V itself.
   DecodeParams dp;
   size_t dsmem = 0;
-  cudaError_t e = make_decode_params(a, ws, true, nullptr, kPrefillSmemLimit, &dp, &dsmem);
+  cudaError_t e = make_decode_params(a, ws, true, write, kPrefillSmemLimit, &dp, &dsmem);
   if (e != cudaSuccess) return e;
   const bool wide = G > 8;
   if (a.head_dim == 128) {

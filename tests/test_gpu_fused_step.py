@@ -1,11 +1,13 @@
 """GPU parity of reshape_and_cache + paged_attention_varlen in one call.
 
-For a bf16 decode-only step the two run as one kernel that writes each
-token's K/V row to its slot and uses it in place of the cache's copy.  Its
-outputs and cache image must equal those of the two separate calls bit for
-bit (the same bf16 values meet the same arithmetic), and match the oracle
-within the bf16 tolerance; other steps (prefill rows, float32) run the two
-kernels one after the other and must equal the separate calls too.
+For bf16 the two run as one kernel.  A decode row's CTA writes the token's
+K/V row to its slot and uses it in place of the cache's copy; the prefill
+CTAs write the rows of their own query tiles and meet at a counter in the
+workspace before reading K/V.  Outputs and cache image must equal those of
+the two separate calls bit for bit (the same bf16 values meet the same
+arithmetic), and match the oracle within the bf16 tolerance; float32 steps
+run the two kernels one after the other and must equal the separate calls
+too.
 """
 
 import math
@@ -105,11 +107,97 @@ def test_fused_decode_random_shapes(case):
 
 
 def test_fused_entry_with_prefill_rows_and_float32():
-    # prefill rows: reshape_and_cache runs first as its own kernel
+    # bf16 prefill rows: one kernel; float32: reshape_and_cache runs first
     b = _batch("fusedmix", 32, 8, 128, [1, 300, 1, 40], [999, 20, 15, 0])
     _check_against_two_calls(b)
     b = _batch("fusedf32", 4, 2, 64, [1, 7, 1], [39, 0, 19], dtype=torch.float32)
     _check_against_two_calls(b)
+
+
+# (H, Hkv, D, query lengths, histories): a 512-token chunk beside decodes, a
+# chunk starting inside a block, prompts only (many prefill CTAs meet), query
+# lengths below one tile's tokens, GQA groups 1 to 16, head_dim 64
+FUSED_MIXED_CASES = [
+    (32, 8, 128, [512] + [1] * 24, [1536] + [int(x) for x in np.linspace(200, 6000, 24)]),
+    (32, 8, 128, [37, 1, 1, 200], [1003, 77, 16, 5]),
+    (32, 8, 128, [300] * 12, [0] * 12),
+    (16, 8, 128, [2, 3, 1, 5], [14, 0, 40, 11]),
+    (8, 8, 64, [130, 1, 64], [60, 500, 0]),
+    (64, 4, 128, [97, 1, 33], [31, 1000, 200]),
+    (16, 1, 64, [250, 1], [1, 3000]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FUSED_MIXED_CASES)))
+def test_fused_mixed_and_prefill_steps(case):
+    H, Hkv, D, qlens, ncs = FUSED_MIXED_CASES[case]
+    b = _batch(f"fusedmixed{case}", H, Hkv, D, qlens, ncs)
+    _check_against_two_calls(b)
+
+
+def test_fused_chunked_prefill_steps_reuse_one_workspace():
+    """A 700-token prompt prefilled in chunks of 256, 256 and 188 while three
+    requests decode, on one cache and one workspace: each step through the
+    fused call against the oracle (the prefill CTAs' meeting counter must be
+    back at zero after every call), then the cache image."""
+    pkv = _pkv()
+    H, Hkv, D, name = 32, 8, 128, "fusedchunks"
+    prompt, chunks = 700, [256, 256, 188]
+    ctx0 = [90, 17, 2500]
+    steps = len(chunks)
+    final = [prompt] + [c + steps - 1 for c in ctx0]
+    R = len(final)
+    counts = [(f + 15) // 16 for f in final]
+    NB = 2 * sum(counts) + 8
+    blocks = random_block_placement(NB, counts, name, "placement")
+    lengths = np.array(final, np.int64)
+    offsets = np.concatenate([[0], np.cumsum(lengths)[:-1]]).astype(np.int64)
+    n = int(lengths.sum())
+    kv = KVHistory(randn_fp32((n, Hkv, D), name, "k", dtype=torch.bfloat16),
+                   randn_fp32((n, Hkv, D), name, "v", dtype=torch.bfloat16), lengths, offsets)
+    qall = randn_fp32((steps, max(chunks) + R - 1, H, D), name, "q", dtype=torch.bfloat16)
+    ws = pkv.new_workspace(R, H, D)
+    cache = None
+    done = 0
+    for s in range(steps):
+        qlens = [chunks[s]] + [1] * (R - 1)
+        ncs = [done] + [c - 1 + s for c in ctx0]
+        b = Batch(kv, blocks, NB, qlens, ncs, qall[s, :sum(qlens)], H, torch.bfloat16)
+        if cache is None:
+            # the decode requests' histories; the prompt has none yet
+            b.alloc_cache().fill_history()
+            cache = (b.key_cache, b.value_cache)
+        b.key_cache, b.value_cache = cache
+        b.upload_metadata()
+        k, v, _ = b.new_tokens()
+        b.k_new, b.v_new = k.to("cuda", b.dtype), v.to("cuda", b.dtype)
+        out, _ = _fused(b, workspace=ws)
+        torch.cuda.synchronize()
+        assert pkv.read_error_word(ws) == 0, s
+        compare(out, b.oracle(), b.qsl_host, b.dtype)
+        # the prefill CTAs' meeting counter (header words 1 and 2) is back at zero
+        assert ws[4:12].count_nonzero().item() == 0, s
+        done += chunks[s]
+    kf = cache[0].view(-1, Hkv, D)
+    slots = [int(blocks[0][p // 16]) * 16 + p % 16 for p in range(prompt)]
+    assert torch.equal(kf[torch.tensor(slots, device="cuda")].cpu(), kv.k(0)[:prompt])
+
+
+def test_fused_prefill_slot_mismatch_sets_metadata_bit():
+    pkv = _pkv()
+    b = _batch("fusedbadp", 32, 8, 128, [1, 40, 1], [40, 17, 300], spare=64)
+    bad = b.slot_mapping.clone()
+    used = set(int(x) for row in b.blocks for x in row)
+    spare_block = next(i for i in range(b.num_blocks) if i not in used)
+    bad[5] = spare_block * 16 + 3  # a token of the prefill row
+    out, ws = _fused(b, slot_mapping=bad)
+    torch.cuda.synchronize()
+    assert pkv.read_error_word(ws) & pkv.ERR_METADATA
+    kf = b.key_cache.view(-1, b.Hkv, b.D)
+    assert torch.equal(kf[bad[5]], b.k_new[5])
+    # the decode requests are unaffected
+    ref = b.oracle()
+    compare(out, ref, b.qsl_host, b.dtype, rows=[0, 2])
 
 
 def test_fused_decode_repeated_steps():
