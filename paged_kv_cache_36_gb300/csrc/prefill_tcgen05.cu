@@ -242,6 +242,13 @@ __device__ __forceinline__ void transpose_lane_groups(uint4 (&v)[NV], int lane) 
   }
 }
 
+// max(a, b, c) in one instruction (the three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // All lanes of the calling warp wait; the result is made warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           volatile int* abort) {
@@ -369,8 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The kernel before this one may still read the caches (or write the new
     // rows): wait for it.  Each CTA writes the rows of its own tiles, then
     // the prefill CTAs meet at a counter in the workspace, so that every
-    // tile's copies find every row of its keys in the cache.  The prefill
-    // CTAs are one per SM and all co-resident; the wait is bounded.
+    // tile's copies find every row of its keys in the cache.  The grid is
+    // one CTA per SM (its registers admit no second one), and the
+    // prefill CTAs have the lowest indices, so all of them are resident once
+    // the kernels before this one drain; the wait is bounded all the same.
     grid_dependency_wait();
     for (int it = 0, ct = cta_tile(0, cid, ncta, total); ct >= 0;
          ct = cta_tile(++it, cid, ncta, total))
@@ -641,10 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 64; ++c)
             if (key0 + c > pos) sv[c] = -INFINITY;
         }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // row max: four chains of three-input maxima
+        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-        for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
-        const float m_mine = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+        for (int c = 4; c < 64; c += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], sv[c + k], sv[c + 4 + k]);
+        const float m_mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
         const float mx = fmaxf(m_mine, exchange(m_mine));  // row max of the key tile
         if (j == 0) {
           m_used = mx;  // finite: key 0 is visible to every row
@@ -680,18 +692,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P = 2^(s * scale_log2 - m_used) as bf16 pairs over the first 32 of
         // this warp's 64 S columns
-        const float neg_m = -m_used;
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        // (two lanes of each packed fma and add: f32x2 operations)
+        const float2 sl2x2 = make_float2(sl2, sl2), neg_m2 = make_float2(-m_used, -m_used);
+        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = exp2_approx(fmaf(sv[2 * e], sl2, neg_m));
-          const float p1 = exp2_approx(fmaf(sv[2 * e + 1], sl2, neg_m));
-          l4[e & 3] += p0 + p1;
-          w[e] = pack_bf16(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(sv[2 * e], sv[2 * e + 1]), sl2x2, neg_m2);
+          const float2 pe = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+          l2[e & 1] = __fadd2_rn(l2[e & 1], pe);
+          w[e] = pack_bf16(pe.x, pe.y);
         }
         tmem_st32(s_cols, w);
-        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        l += (l2[0].x + l2[1].x) + (l2[0].y + l2[1].y);
         tmem_wait_st();
         // keys past the tile's last row were not loaded: zero their V rows
         // so that 0 * (stale) stays 0
