@@ -21,6 +21,7 @@ __all__ = [
     "PkvError", "lib", "reshape_and_cache", "rope_reshape_and_cache", "copy_blocks",
     "attention_workspace_bytes", "new_workspace",
     "paged_attention_varlen", "reshape_and_cache_paged_attention", "read_error_word",
+    "PreparedCall", "prepare_reshape_and_cache_paged_attention",
     "build_slot_mapping", "Allocator", "Scheduler",
 ]
 
@@ -217,6 +218,55 @@ def reshape_and_cache_paged_attention(key, value, slot_mapping, q, key_cache, va
         int(max_query_len), workspace.data_ptr(), workspace.nbytes, _stream_ptr(stream))
     _check(code, "reshape_and_cache_paged_attention")
     return out
+
+
+class PreparedCall:
+    """A C-ABI call whose arguments were marshalled once.  Calling it makes the
+    same library call again, on the stream resolved at preparation: for a
+    serving loop whose buffers stay in place from step to step, this leaves
+    out the per-call Python work (pointer, stride and stream lookups).  The
+    library still validates every call.  The tensors it was prepared from are
+    kept alive; their storage and shapes must not change."""
+
+    __slots__ = ("_fn", "_args", "_keep", "_where")
+
+    def __init__(self, fn, args, keep, where):
+        self._fn, self._args, self._keep, self._where = fn, args, keep, where
+
+    def __call__(self):
+        code = self._fn(*self._args)
+        if code < 0:
+            raise PkvError(code, self._where)
+        return self._keep[0]
+
+
+def prepare_reshape_and_cache_paged_attention(key, value, slot_mapping, q, key_cache,
+                                              value_cache, block_table, query_start_loc,
+                                              seq_lens, num_computed_tokens, scale: float, out,
+                                              workspace, max_query_len: int = 0, stream=None):
+    """reshape_and_cache_paged_attention with its arguments marshalled once;
+    returns a PreparedCall that issues the call (and returns out) each time it
+    is called.  out and workspace are required: they are part of the state the
+    calls reuse."""
+    import torch
+    T, H, D = q.shape
+    nb, bs, hkv, _ = key_cache.shape
+    R = int(seq_lens.shape[0])
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    args = (key.data_ptr(), _token_stride(key), value.data_ptr(), _token_stride(value),
+            slot_mapping.data_ptr(), q.data_ptr(), _token_stride(q), key_cache.data_ptr(),
+            value_cache.data_ptr(), block_table.data_ptr(), _row_stride(block_table),
+            query_start_loc.data_ptr(), seq_lens.data_ptr(), num_computed_tokens.data_ptr(),
+            float(scale), out.data_ptr(), _token_stride(out), T, R, nb, bs, H, hkv, D,
+            _dtype_code(q), int(max_query_len), workspace.data_ptr(), workspace.nbytes,
+            _stream_ptr(stream))
+    keep = (out, key, value, slot_mapping, q, key_cache, value_cache, block_table,
+            query_start_loc, seq_lens, num_computed_tokens, workspace)
+    return PreparedCall(lib().pkv_reshape_and_cache_paged_attention, args, keep,
+                        "reshape_and_cache_paged_attention")
 
 
 # ---------------------------------------------------------------------------

@@ -86,3 +86,39 @@ def test_rope_argument_checks(libpkv):
     assert call(rd=8, neox=0) == 0                       # interleaved 8 bf16 = 16 bytes
     assert call(T=3) == -1                               # null pointers with tokens to do
     assert b"null pointer" in lib.pkv_last_error()
+
+
+def test_prepared_call_matches_the_eager_call_without_gpu(libpkv):
+    """The prepared form passes the same arguments as the eager binding: on a
+    machine without a GPU both fail the same way (block_size 8 is refused
+    before any CUDA call), and the prepared call raises on every call."""
+    import torch
+    import paged_kv_cache_36_gb300 as pkv
+    T, H, Hkv, D, R, NB = 4, 8, 2, 64, 2, 16
+    q = torch.zeros(T, H, D, dtype=torch.bfloat16)
+    kc = torch.zeros(NB, 8, Hkv, D, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    k = torch.zeros(T, Hkv, D, dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    slots = torch.zeros(T, dtype=torch.int64)
+    bt = torch.zeros(R, 4, dtype=torch.int32)
+    qsl = torch.tensor([0, 2, 4], dtype=torch.int32)
+    seq = torch.tensor([2, 2], dtype=torch.int32)
+    nc = torch.zeros(R, dtype=torch.int32)
+    out = torch.empty_like(q)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+
+    class _S:  # a stand-in stream object (no CUDA here)
+        cuda_stream = 0
+
+    args = (k, v, slots, q, kc, vc, bt, qsl, seq, nc, 0.125)
+    with pytest.raises(pkv.PkvError) as eager:
+        pkv.reshape_and_cache_paged_attention(*args, out=out, workspace=ws, max_query_len=2,
+                                              stream=_S())
+    call = pkv.prepare_reshape_and_cache_paged_attention(*args, out=out, workspace=ws,
+                                                         max_query_len=2, stream=_S())
+    for _ in range(2):
+        with pytest.raises(pkv.PkvError) as prepared:
+            call()
+        assert prepared.value.code == eager.value.code
+        assert "block_size" in str(prepared.value)
