@@ -214,8 +214,11 @@ int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void
  * block_size + j % block_size.  seq_lens[r] must equal num_computed_tokens[r]
  * + query length (the KV length after this step's reshape_and_cache), so the
  * keys of this step's own tokens must already be in the cache.
- * Requests with query length 1 run on the split-KV decode kernel, longer ones
- * on the chunked-prefill kernel; query length 0 contributes no rows.
+ * A bf16 call is one kernel: with only query-length-1 rows the split-KV
+ * decode kernel; otherwise one persistent kernel whose CTAs split the SMs on
+ * the device between the chunked-prefill tiles of the longer rows and the
+ * split-KV decode of the query-length-1 rows.  Query length 0 contributes
+ * no rows.
  *
  * q, out: device [num_tokens, num_heads, head_dim], token stride q_stride /
  *   out_stride elements, heads and dims contiguous.
@@ -225,7 +228,8 @@ int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void
  *   [num_reqs] = num_tokens.  seq_lens, num_computed_tokens: device int32
  *   [num_reqs].
  * max_query_len: host hint, >= every request's query length, or 0 if
- *   unknown; a value <= 1 skips the prefill launch.
+ *   unknown; a value of 1 launches the decode-only kernel (rows longer than
+ *   one token are then not computed).
  * workspace: device scratch of at least pkv_attention_workspace_bytes()
  *   bytes for this batch, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves
  *   it ready for the next one, including calls with a different number of
