@@ -77,7 +77,6 @@ struct DecodeParams {
   float* part_o;
   float* part_ml;
   uint32_t* err;
-  int32_t wait_before_loads;  // wait for the preceding grid before reading Q or the caches
   int32_t stages;
   uint32_t stage_bytes;
   // Fused reshape_and_cache (k_new == nullptr: off).  Each decode token's new
@@ -94,10 +93,9 @@ struct DecodeParams {
 
 // Fills the decode parameters of a call and the dynamic shared memory a CTA
 // needs (as many K/V stages as fit in smem_budget, at most kDecodeMaxStages).
-// wait_before_loads: the kernel reads Q and the caches only after the grid
-// before it has completed.  write: fused reshape_and_cache, or null.
+// write: fused reshape_and_cache, or null.
 inline cudaError_t make_decode_params(const AttnArgs& a, const DecodeScratch& ws,
-                                      bool wait_before_loads, const CacheWrite* write,
+                                      const CacheWrite* write,
                                       size_t smem_budget, DecodeParams* out, size_t* smem) {
   if (a.num_reqs > kDecodeMaxReqs || a.num_kv_heads > 8) return cudaErrorNotSupported;
   DecodeParams prm;
@@ -121,7 +119,6 @@ inline cudaError_t make_decode_params(const AttnArgs& a, const DecodeScratch& ws
   prm.part_o = ws.part_o;
   prm.part_ml = ws.part_ml;
   prm.err = a.err;
-  prm.wait_before_loads = wait_before_loads ? 1 : 0;
   prm.k_new = write ? static_cast<const __nv_bfloat16*>(write->key) : nullptr;
   prm.v_new = write ? static_cast<const __nv_bfloat16*>(write->value) : nullptr;
   prm.k_new_stride = write ? write->key_stride : 0;
@@ -240,12 +237,10 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& kmap, const CUtens
   if (warp == hkv) {
     // ======================= producer warp =======================
     // Launched as a programmatic dependent, this grid may run its prologue
-    // while the kernel before it finishes.  When that kernel may be the cache
-    // write (with or without RoPE, which also rewrites Q), the caches and Q
-    // are read only after it has completed.  After the prefill kernel there
-    // is nothing to wait for here: it writes nothing this grid reads, and it
-    // releases this grid only once it has seen the cache write complete.
-    if (p.wait_before_loads) grid_dependency_wait();
+    // while the kernel before it finishes.  That kernel may be the cache
+    // write (with or without RoPE, which also rewrites Q), so the caches and
+    // Q are read only after it has completed.
+    grid_dependency_wait();
     int stage = 0;
     uint32_t phase = 0;
     int r = r0;
@@ -295,7 +290,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& kmap, const CUtens
   // ======================= consumer warps (one per KV head) =======================
   // Q may still be being rotated in place by the preceding kernel (see the
   // producer's wait above)
-  if (p.wait_before_loads) grid_dependency_wait();
+  grid_dependency_wait();
   const int h = warp;
   const int G = p.group;
   const int gid = lane >> 2, tid = lane & 3;

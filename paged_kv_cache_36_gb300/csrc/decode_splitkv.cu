@@ -54,7 +54,7 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const CUtensorMap& kmap, const
   if (a.num_reqs == 0) return cudaSuccess;
   DecodeParams prm;
   size_t smem = 0;
-  const cudaError_t e = make_decode_params(a, ws, true, write, kSmemBudget, &prm, &smem);
+  const cudaError_t e = make_decode_params(a, ws, write, kSmemBudget, &prm, &smem);
   if (e != cudaSuccess) return e;
   const bool wide = prm.group > 8;
   if (a.head_dim == 128)

@@ -856,7 +856,7 @@ cudaError_t launch_varlen_bf16(const AttnArgs& a, const CUtensorMap& qmap, const
   // role, so it waits for it too; it writes the decode rows' new K/V itself.
   DecodeParams dp;
   size_t dsmem = 0;
-  cudaError_t e = make_decode_params(a, ws, true, write, kPrefillSmemLimit, &dp, &dsmem);
+  cudaError_t e = make_decode_params(a, ws, write, kPrefillSmemLimit, &dp, &dsmem);
   if (e != cudaSuccess) return e;
   const bool wide = G > 8;
   if (a.head_dim == 128) {
