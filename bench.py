@@ -255,9 +255,13 @@ def build_decode_steps(pkv, device, replicas=4):
     return cfg, steps
 
 
-def build_mixed_step(pkv, device):
+def build_mixed_step(pkv, device, with_prefill_alone=False, **mix):
+    """The mixed chunked-prefill step (config 3 by default, or the mix the
+    keyword arguments of configs.mixed_chunked_step give) as one fused call,
+    the same step's decodes alone and, on request, its prefill request
+    alone."""
     from workloads import configs
-    cfg = configs.mixed_chunked_step()
+    cfg = configs.mixed_chunked_step(**mix)
     shape = (cfg.num_blocks, 16, cfg.num_kv_heads, cfg.head_dim)
     kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
     vc = torch.empty_like(kc)
@@ -286,7 +290,12 @@ def build_mixed_step(pkv, device):
     # each step is one call of the fused entry: the cache write and the
     # attention in one kernel
     step.fuse = decodes.fuse = True
-    return cfg, step, decodes
+    if not with_prefill_alone:
+        return cfg, step, decodes
+    prefill = DeviceStep(pkv, kc, vc, cfg.q[:q0], knew[0], vnew[0], cfg.blocks[:1],
+                         cfg.query_len[:1], cfg.num_computed[:1], cfg.num_heads, device)
+    prefill.fuse = True
+    return cfg, step, decodes, prefill
 
 
 def build_prefill_chunks(pkv, device, copies=CHUNK_COPIES, pool_blocks=4096, from_start=False):
@@ -829,6 +838,32 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     }
     del kc, vc, ws
     torch.cuda.empty_cache()
+    # ---- the mixed batch as one kernel on two other mixes: the step against
+    # its decodes alone and its prefill request alone (each one fused call
+    # per step, eager, back to back) ----
+    mixes = {
+        "prefill_heavy": dict(num_decodes=64, chunk_start=0, chunk_end=2048, ctx_lo=128,
+                              ctx_hi=4096, pool=65536),
+        "small_chunk": dict(num_decodes=256, chunk_start=1920, chunk_end=2048),
+    }
+    res["mixed_batches"] = {}
+    for name, mix in mixes.items():
+        _, mstep, mdec, mpre = build_mixed_step(pkv, device, with_prefill_alone=True, **mix)
+        times = {}
+        for key, obj in (("mixed", mstep), ("decodes_alone", mdec), ("prefill_alone", mpre)):
+            for _ in range(5):
+                obj.step()
+            tot, _ = time_loop([obj], 40, stream)
+            times[key] = tot / 40
+        res["mixed_batches"][name] = {
+            "workload": f"{mix['chunk_end'] - mix['chunk_start']}-token chunk at "
+                        f"[{mix['chunk_start']},{mix['chunk_end']}) + {mix['num_decodes']} decodes",
+            "ms_per_step": times["mixed"], "decodes_alone_ms": times["decodes_alone"],
+            "prefill_alone_ms": times["prefill_alone"],
+            "sum_of_parts_ms": times["decodes_alone"] + times["prefill_alone"],
+        }
+        del mstep, mdec, mpre
+        torch.cuda.empty_cache()
     return res
 
 
