@@ -21,7 +21,8 @@
 // SMs than on all 152, and the prefill then ends well inside the step), and
 // capped so that the decode keeps 67 SMs.  When the prefill cannot finish
 // within half the decode's time on the SMs it may take, the SMs are split in
-// proportion to each role's time on one SM.  Each role keeps at least one
+// proportion to each role's time on one SM (a decode SM beside a busy
+// prefill streams about 70 bytes/ns).  Each role keeps at least one
 // CTA while it has rows, so that rows with bad metadata are still reported.
 #pragma once
 
@@ -98,7 +99,8 @@ __device__ __forceinline__ int mixed_prefill_ctas(const MixedWork& w, int sms) {
   if (w.decode_rows == 0 || sms < 2) return sms;
   if (w.prefill_tiles == 0) return 1;  // only rows that fail their checks
   if (w.decode_bytes == 0) return sms - 1;
-  constexpr unsigned long long kHbmBytesPerNs = 7000, kSmBytesPerNs = 105, kSatSms = 67;
+  // the decode saturates HBM (7000 bytes/ns) from about 67 SMs (105 bytes/ns each)
+  constexpr unsigned long long kHbmBytesPerNs = 7000, kSatSms = 67;
   const unsigned long long t_d = w.decode_bytes / kHbmBytesPerNs;
   const unsigned long long tile_ns =
       (w.prefill_units * 1100 + w.prefill_tiles * 3000) * 13 / (10 * w.prefill_tiles);
@@ -112,8 +114,10 @@ __device__ __forceinline__ int mixed_prefill_ctas(const MixedWork& w, int sms) {
       return n > floor_share ? n : (floor_share > 0 ? floor_share : 1);
     }
   }
-  // prefill-heavy: split by each kernel's time on one SM
-  const unsigned long long t_d1 = w.decode_bytes / kSmBytesPerNs;
+  // prefill-heavy: split by each role's time on one SM (a decode SM beside
+  // a busy prefill streams about 70 bytes/ns)
+  constexpr unsigned long long kMixedSmBytesPerNs = 70;
+  const unsigned long long t_d1 = w.decode_bytes / kMixedSmBytesPerNs;
   const unsigned long long t_p1 = w.prefill_tiles * tile_ns;
   unsigned long long m = (static_cast<unsigned long long>(sms) * t_d1 + t_d1 + t_p1 - 1) /
                          (t_d1 + t_p1);  // decode SMs, rounded up
