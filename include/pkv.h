@@ -234,8 +234,10 @@ int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void
  *   bytes for this batch, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves
  *   it ready for the next one, including calls with a different number of
  *   requests (its layout follows the largest batch it can hold).  Word 0 is
- *   the error word (PKV_ERR_* bits, OR-ed in).  Two calls that overlap on the
- *   GPU must not share a workspace.
+ *   the error word (PKV_ERR_* bits, OR-ed in).  A call that reports
+ *   PKV_ERR_TIMEOUT may leave its counters set: zero the workspace again
+ *   before reusing it.  Two calls that overlap on the GPU must not share a
+ *   workspace.
  * Ordering: the kernels are launched as programmatic dependents of the
  * kernel before the call on `stream`, so their set-up overlaps its tail.
  * They read q and the caches and write out and the workspace only after that
