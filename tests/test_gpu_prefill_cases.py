@@ -72,3 +72,29 @@ def test_prefill_across_group_sizes(H, Hkv, D):
 def _pkv():
     import paged_kv_cache_36_gb300 as pkv
     return pkv
+
+
+@pytest.mark.parametrize("bad", ["prefill_row", "only_prefill_row", "decode_row"])
+def test_mixed_call_with_a_bad_row(bad):
+    """One kernel serves both kinds of rows: a row whose seq_len disagrees with
+    num_computed + query length sets the metadata bit and is skipped, and the
+    other rows still match the oracle (whichever role the bad row belongs to,
+    including a call whose only prefill row is bad)."""
+    pkv = _pkv()
+    if bad == "only_prefill_row":
+        qlens, ncs, victim = [1, 200, 1], [700, 300, 90], 1
+    elif bad == "prefill_row":
+        qlens, ncs, victim = [1, 200, 64, 1], [700, 300, 1000, 90], 1
+    else:
+        qlens, ncs, victim = [1, 200, 64, 1], [700, 300, 1000, 90], 3
+    b = _batch(f"badrow_{bad}", qlens, ncs)
+    ref = b.oracle()
+    b.seq_lens[victim] += 3
+    ws = pkv.new_workspace(b.R, b.H, b.D)
+    out = pkv.paged_attention_varlen(b.q, b.key_cache, b.value_cache, b.block_table, b.qsl,
+                                     b.seq_lens, b.nc, 1.0 / np.sqrt(b.D), workspace=ws,
+                                     max_query_len=int(max(qlens)))
+    torch.cuda.synchronize()
+    assert pkv.read_error_word(ws) & pkv.ERR_METADATA
+    rows = [r for r in range(b.R) if r != victim]
+    compare(out, ref, b.qsl_host, torch.bfloat16, rows=rows)
