@@ -35,6 +35,7 @@ from __future__ import annotations
 
 import argparse
 import functools
+import gc
 import hashlib
 import json
 import math
@@ -1229,10 +1230,26 @@ def main():
     for i in range(args.warmup):
         e2e_step(i)
     e2e_n = 3 if args.profile else max(50, min(args.steps, 1000))
-    t0 = time.perf_counter()
-    for i in range(e2e_n):
-        e2e_step(args.warmup + i)
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_n
+    step_ends = [0.0] * (e2e_n + 1)
+    # the collector runs before the timed steps and not during them (as
+    # timeit does): a full pass over the interpreter's objects takes a few
+    # hundred ms, which would land on whichever step triggered it
+    gc.collect()
+    gc.disable()
+    try:
+        t0 = step_ends[0] = time.perf_counter()
+        for i in range(e2e_n):
+            e2e_step(args.warmup + i)
+            step_ends[i + 1] = time.perf_counter()
+    finally:
+        gc.enable()
+    e2e_ms = (step_ends[-1] - t0) * 1e3 / e2e_n
+    # each step's wall time, so that a stall of the host shows as one slow
+    # step rather than as a slower mean
+    walls = np.sort(np.diff(np.array(step_ends)) * 1e3)
+    e2e_spread = {"median_ms": float(walls[len(walls) // 2]),
+                  "p99_ms": float(walls[min(len(walls) - 1, int(len(walls) * 0.99))]),
+                  "max_ms": float(walls[-1]), "steps": e2e_n}
     e2e_ms, e2e_bytes = combine_ranks(e2e_ms, float(step_bytes), dist, device)
     e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
     # The same step with its device work (H2D, the call, D2H) captured once in
@@ -1261,10 +1278,15 @@ def main():
 
         for _ in range(args.warmup):
             e2e_graph_step()
-        t0 = time.perf_counter()
-        for _ in range(e2e_n):
-            e2e_graph_step()
-        gms = (time.perf_counter() - t0) * 1e3 / e2e_n
+        gc.collect()
+        gc.disable()
+        try:
+            t0 = time.perf_counter()
+            for _ in range(e2e_n):
+                e2e_graph_step()
+            gms = (time.perf_counter() - t0) * 1e3 / e2e_n
+        finally:
+            gc.enable()
         gms, gbytes = combine_ranks(gms, float(step_bytes), dist, device)
         e2e_graph = {"value": gbytes / (gms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": gms,
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -1354,8 +1376,9 @@ def main():
                                 "stream after the host built its slot_mapping; the call in the "
                                 "binding's prepared form) -> the next step's "
                                 "slot_mapping and H2D while this one runs -> D2H out -> stream "
-                                "sync; K H2D and K D2H copies in K timed steps",
-                        "graph": e2e_graph},
+                                "sync; K H2D and K D2H copies in K timed steps; Python's cyclic "
+                                "collector run before the timed steps and off during them",
+                        "step_wall_times": e2e_spread, "graph": e2e_graph},
                 "secondary": secondary,
                 "extra": extra,
                 "cpu_baseline": cpu,
