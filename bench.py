@@ -454,17 +454,12 @@ def event_time(fn, n, stream):
     return a.elapsed_time(b) / n
 
 
-def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
-    """Supporting measurements beside the headline: the long-context decode
-    (config 4), the continuous-batching trace (config 5) per step,
-    reshape_and_cache at 8192 tokens with and without the fused RoPE of Q and
-    K, and the prefill kernel on a 2048-token prompt, on 8 such prompts in one
-    call and on one 16384-token prompt."""
-    from workloads import configs, trace_spec, generate_arrivals
-    from workloads.generators import random_block_placement
-    res = {}
-    # ---- config 4: 8 decodes over 131072-token histories, 2^20-block pool ----
-    cfg = configs.long_decode_llama70b()
+def build_long_decode(pkv, device, pool=1 << 20):
+    """Config 4's decode call: 8 decodes over 131072-token histories,
+    Llama-3-70B heads (64/8/128), blocks scattered over a pool of `pool`
+    blocks (2^20 = 68.7 GB by default); only the used blocks are filled."""
+    from workloads import configs
+    cfg = configs.long_decode_llama70b(pool=pool)
     H, Hkv, D = cfg.num_heads, cfg.num_kv_heads, cfg.head_dim
     nb = cfg.num_blocks
     kc = torch.empty((nb, 16, Hkv, D), dtype=torch.bfloat16, device=device)
@@ -480,6 +475,20 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     q = torch.randn((R, H, D), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
     step = DeviceStep(pkv, kc, vc, q.cpu(), q.cpu()[:, :Hkv], q.cpu()[:, :Hkv], cfg.blocks,
                       np.ones(R, np.int64), cfg.context - 1, H, device)
+    return kc, vc, step
+
+
+def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
+    """Supporting measurements beside the headline: the long-context decode
+    (config 4), the continuous-batching trace (config 5) per step,
+    reshape_and_cache at 8192 tokens with and without the fused RoPE of Q and
+    K, and the prefill kernel on a 2048-token prompt, on 8 such prompts in one
+    call and on one 16384-token prompt."""
+    from workloads import configs, trace_spec, generate_arrivals
+    from workloads.generators import random_block_placement
+    res = {}
+    # ---- config 4: 8 decodes over 131072-token histories, 2^20-block pool ----
+    kc, vc, step = build_long_decode(pkv, device)
     for _ in range(3):
         step.attn()
     ms = event_time(step.attn, 20, stream)
@@ -490,7 +499,7 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
         "frac_of_hbm_peak": step.decode_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
         "algorithmic_bytes_per_launch": step.decode_bytes,
     }
-    del kc, vc, step, used
+    del kc, vc, step
     torch.cuda.empty_cache()
     # ---- reshape_and_cache at 8192 tokens (inputs rotate over 4 batches) ----
     T, Hkv, D = 8192, 8, 128
@@ -1002,6 +1011,10 @@ def main():
     ap.add_argument("--profile-k1", action="store_true",
                     help="only --steps reshape_and_cache calls of 8192 tokens (4 rotating "
                          "batches), for ncu")
+    ap.add_argument("--profile-long-decode", action="store_true",
+                    help="only --steps decode calls of config 4's requests (8 x 131072-token "
+                         "contexts, Llama-3-70B heads) in a pool that just holds them "
+                         "(66560 blocks, 4.4 GB), for ncu")
     ap.add_argument("--profile-copy", action="store_true",
                     help="only --steps copy_blocks calls of 4096 scattered block pairs within "
                          "a 16384-block pool, for ncu")
@@ -1088,6 +1101,16 @@ def main():
                 pkv.copy_blocks(kc, vc, kc, vc, pairs, error_word=err)
         torch.cuda.synchronize()
         print(json.dumps({"profile_calls": args.warmup + args.steps, "error_word": int(err.item())}))
+        return
+
+    if args.profile_long_decode:
+        _, _, step = build_long_decode(pkv, device, pool=8 * 131072 // 16 + 1024)
+        for _ in range(args.warmup + args.steps):
+            step.attn()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_long_decode_calls": args.warmup + args.steps,
+                          "algorithmic_bytes_per_launch": step.decode_bytes,
+                          "error_word": pkv.read_error_word(step.ws)}))
         return
 
     if args.profile_mixed:
