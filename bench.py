@@ -351,6 +351,30 @@ def _cudart():
     return None
 
 
+def host_mapped(t) -> bool:
+    """True when the CUDA runtime reports t's storage as host memory that the
+    device addresses at the same pointer (pinned memory under unified
+    addressing), so a kernel may store to it."""
+    import ctypes
+
+    class Attr(ctypes.Structure):
+        # cudaPointerAttributes: type, device, devicePointer, hostPointer and
+        # long reserved[8], with spare room past it
+        _fields_ = [("type", ctypes.c_int), ("device", ctypes.c_int),
+                    ("devicePointer", ctypes.c_void_p), ("hostPointer", ctypes.c_void_p),
+                    ("reserved", ctypes.c_long * 8), ("spare", ctypes.c_char * 256)]
+
+    rt = _cudart()
+    if rt is None:
+        return False
+    rt.cudaPointerGetAttributes.argtypes = [ctypes.POINTER(Attr), ctypes.c_void_p]
+    rt.cudaPointerGetAttributes.restype = ctypes.c_int
+    a = Attr()
+    if rt.cudaPointerGetAttributes(ctypes.byref(a), ctypes.c_void_p(t.data_ptr())) != 0:
+        return False
+    return a.type == 1 and a.devicePointer == t.data_ptr()  # cudaMemoryTypeHost
+
+
 def cuda_copy_async():
     """copy(dst, src, nbytes, stream) of two tensors, one of them pinned host
     memory: cudaMemcpyAsync through the CUDA runtime (cudaMemcpyDefault
@@ -457,7 +481,9 @@ def event_time(fn, n, stream):
 def build_long_decode(pkv, device, pool=1 << 20):
     """Config 4's decode call: 8 decodes over 131072-token histories,
     Llama-3-70B heads (64/8/128), blocks scattered over a pool of `pool`
-    blocks (2^20 = 68.7 GB by default); only the used blocks are filled."""
+    blocks (2^20 = 68.7 GB by default); only the used blocks are filled.
+    Returns the caches, the step and the generator that filled them (later
+    measurements draw from it)."""
     from workloads import configs
     cfg = configs.long_decode_llama70b(pool=pool)
     H, Hkv, D = cfg.num_heads, cfg.num_kv_heads, cfg.head_dim
@@ -475,7 +501,7 @@ def build_long_decode(pkv, device, pool=1 << 20):
     q = torch.randn((R, H, D), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
     step = DeviceStep(pkv, kc, vc, q.cpu(), q.cpu()[:, :Hkv], q.cpu()[:, :Hkv], cfg.blocks,
                       np.ones(R, np.int64), cfg.context - 1, H, device)
-    return kc, vc, step
+    return kc, vc, step, g
 
 
 def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
@@ -488,7 +514,7 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     from workloads.generators import random_block_placement
     res = {}
     # ---- config 4: 8 decodes over 131072-token histories, 2^20-block pool ----
-    kc, vc, step = build_long_decode(pkv, device)
+    kc, vc, step, g = build_long_decode(pkv, device)
     for _ in range(3):
         step.attn()
     ms = event_time(step.attn, 20, stream)
@@ -1104,7 +1130,7 @@ def main():
         return
 
     if args.profile_long_decode:
-        _, _, step = build_long_decode(pkv, device, pool=8 * 131072 // 16 + 1024)
+        _, _, step, _ = build_long_decode(pkv, device, pool=8 * 131072 // 16 + 1024)
         for _ in range(args.warmup + args.steps):
             step.attn()
         torch.cuda.synchronize()
@@ -1187,10 +1213,13 @@ def main():
     # ---- end to end through the public API, from pinned host buffers ----
     # The step's inputs (q, the new K/V rows, block table, query_start_loc,
     # seq_lens, num_computed and the slot mapping built on the host) sit in one
-    # pinned staging buffer and go to the device in one copy; the output comes
-    # back in one copy.  Two staging buffers (host and device) alternate: while
-    # the GPU runs step i, the host builds step i + 1's slot mapping and the
-    # copy of step i + 1's inputs runs on a second stream.
+    # pinned staging buffer and go to the device in one copy.  Two staging
+    # buffers (host and device) alternate: while the GPU runs step i, the host
+    # builds step i + 1's slot mapping and the copy of step i + 1's inputs runs
+    # on a second stream.  The output goes to pinned host memory: the kernel
+    # stores it there itself over the host link when the device maps that
+    # memory at its host address (GB300's Grace host), else one D2H copy
+    # brings it back.
     s0 = steps[0]
     parts = [("q", s0.q.cpu()), ("k_new", s0.k_new.cpu()), ("v_new", s0.v_new.cpu()),
              ("bt", torch.from_numpy(s0.bt_host)), ("qsl", torch.from_numpy(s0.qsl_host)),
@@ -1216,6 +1245,7 @@ def main():
         for name, t in parts[:-1]:
             host[name].copy_(t)
     out_host = torch.empty_like(hosts[0]["q"]).pin_memory()
+    out_direct = host_mapped(out_host)
     h2d = total
     d2h = out_host.numel() * out_host.element_size()
     slots_outs = [host["slots"].numpy() for host in hosts]
@@ -1236,17 +1266,20 @@ def main():
     # binding's prepared form; the library validates every call)
     calls = [pkv.prepare_reshape_and_cache_paged_attention(
         d["k_new"], d["v_new"], d["slots"], d["q"], s0.kc, s0.vc, d["bt"], d["qsl"], d["seq"],
-        d["nc"], s0.scale, out=s0.out, workspace=s0.ws, max_query_len=1, stream=e2e_stream)
+        d["nc"], s0.scale, out=out_host if out_direct else s0.out, workspace=s0.ws,
+        max_query_len=1, stream=e2e_stream)
         for d in devs]
 
     def e2e_step(i):
         # step i's call once its inputs have landed, then step i + 1's inputs
-        # staged while the GPU runs it, then the D2H of out and a sync
+        # staged while the GPU runs it, then (unless the kernel wrote out to
+        # host memory itself) the D2H of out, and a sync
         b = i & 1
         e2e_stream.wait_event(h2d_done[b])
         calls[b]()
         stage_in(i + 1)
-        copy_async(out_host, s0.out, d2h, e2e_stream)
+        if not out_direct:
+            copy_async(out_host, s0.out, d2h, e2e_stream)
         e2e_stream.synchronize()
 
     stage_in(0)
@@ -1398,9 +1431,13 @@ def main():
                                 "holding all of them, issued during the previous step on a copy "
                                 "stream after the host built its slot_mapping; the call in the "
                                 "binding's prepared form) -> the next step's "
-                                "slot_mapping and H2D while this one runs -> D2H out -> stream "
-                                "sync; K H2D and K D2H copies in K timed steps; Python's cyclic "
-                                "collector run before the timed steps and off during them",
+                                "slot_mapping and H2D while this one runs -> out into pinned "
+                                "host memory -> stream sync; K H2D copies in K timed steps; "
+                                "Python's cyclic collector run before the timed steps and off "
+                                "during them",
+                        "out_to_host": ("stored by the kernel into device-mapped pinned host "
+                                        "memory over the host link (no D2H copy)"
+                                        if out_direct else "one D2H copy per step"),
                         "step_wall_times": e2e_spread, "graph": e2e_graph},
                 "secondary": secondary,
                 "extra": extra,

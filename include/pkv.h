@@ -220,8 +220,13 @@ int pkv_copy_blocks(const void* src_key_cache, const void* src_value_cache, void
  * split-KV decode of the query-length-1 rows.  Query length 0 contributes
  * no rows.
  *
- * q, out: device [num_tokens, num_heads, head_dim], token stride q_stride /
- *   out_stride elements, heads and dims contiguous.
+ * q, out: [num_tokens, num_heads, head_dim], token stride q_stride /
+ *   out_stride elements, heads and dims contiguous.  q is device memory.
+ *   out is device memory, or pinned host memory that the device addresses
+ *   at its host pointer (cudaHostAlloc / cudaMallocHost memory under unified
+ *   addressing): the kernels only store to out and never read it, so a host
+ *   buffer receives the result over the host link with no separate copy.
+ *   The call does not check which kind out is.
  * block_table: device int32 [num_reqs, block_table_stride], row-major; only
  *   the first ceil(seq_lens[r] / block_size) entries of row r are read.
  * query_start_loc: device int32 [num_reqs + 1], non-decreasing, [0] = 0,

@@ -170,7 +170,8 @@ def paged_attention_varlen(q, key_cache, value_cache, block_table, query_start_l
     """Causal GQA attention of the flattened batch q [T, H, D] over the paged caches.
 
     block_table int32 [R, max_blocks]; query_start_loc int32 [R + 1]; seq_lens,
-    num_computed_tokens int32 [R].  Returns out [T, H, D].
+    num_computed_tokens int32 [R].  Returns out [T, H, D]: a CUDA tensor, or
+    a pinned CPU tensor that the kernels store into directly.
     """
     import torch
     T, H, D = q.shape
@@ -195,8 +196,9 @@ def reshape_and_cache_paged_attention(key, value, slot_mapping, q, key_cache, va
                                       scale: float, out=None, workspace=None,
                                       max_query_len: int = 0, stream=None):
     """reshape_and_cache of key/value [T, Hkv, D] at slot_mapping (int64 [T]),
-    then paged_attention_varlen of q [T, H, D]; one fused kernel for a bf16
-    decode-only step (max_query_len == 1).  Returns out [T, H, D]."""
+    then paged_attention_varlen of q [T, H, D]; one kernel for any bf16
+    step.  Returns out [T, H, D]: a CUDA tensor, or a pinned CPU tensor that
+    the kernels store into directly."""
     import torch
     T, H, D = q.shape
     nb, bs, hkv, _ = key_cache.shape

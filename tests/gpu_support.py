@@ -155,3 +155,33 @@ def compare(got: torch.Tensor, ref: torch.Tensor, qsl, dtype, rows=None):
             assert d.abs().max().item() <= BF16_MAX_ABS, (r, d.abs().max().item())
             assert (torch.linalg.norm(d) / torch.linalg.norm(ref[a:b])).item() <= BF16_REL, r
     return max_abs, rel
+
+
+def host_buffer_is_device_mapped(t: torch.Tensor) -> bool:
+    """True when the CUDA runtime reports t's storage as host memory that the
+    device addresses at the same pointer (pinned memory under unified
+    addressing), so a kernel may store to it."""
+    import ctypes
+
+    class _Attr(ctypes.Structure):
+        # cudaPointerAttributes: type, device, devicePointer, hostPointer and
+        # long reserved[8], with spare room past it
+        _fields_ = [("type", ctypes.c_int), ("device", ctypes.c_int),
+                    ("devicePointer", ctypes.c_void_p), ("hostPointer", ctypes.c_void_p),
+                    ("reserved", ctypes.c_long * 8), ("spare", ctypes.c_char * 256)]
+
+    rt = None
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if rt is None:
+        return False
+    rt.cudaPointerGetAttributes.argtypes = [ctypes.POINTER(_Attr), ctypes.c_void_p]
+    rt.cudaPointerGetAttributes.restype = ctypes.c_int
+    a = _Attr()
+    if rt.cudaPointerGetAttributes(ctypes.byref(a), ctypes.c_void_p(t.data_ptr())) != 0:
+        return False
+    return a.type == 1 and a.devicePointer == t.data_ptr()  # cudaMemoryTypeHost

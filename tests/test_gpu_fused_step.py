@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_support import Batch, compare
+from tests.gpu_support import Batch, compare, host_buffer_is_device_mapped
 from workloads import configs
 from workloads.configs import KVHistory
 from workloads.generators import randn_fp32, random_block_placement
@@ -253,3 +253,41 @@ def test_fused_decode_slot_mismatch_sets_metadata_bit():
     # the other requests are unaffected
     ref = b.oracle()
     compare(out, ref, b.qsl_host, b.dtype, rows=[0, 2])
+
+
+@pytest.mark.parametrize("kind", ["decode", "mixed", "float32"])
+def test_fused_step_writes_out_into_pinned_host_memory(kind):
+    """out may be pinned host memory that the device maps at its host address:
+    the kernels only store to out, so the result lands in host memory without
+    a device-to-host copy.  The same step with out on the device and with out
+    in pinned host memory: equal bit for bit, and within the oracle's
+    tolerance (the decode kernel, the mixed-batch kernel with both roles, and
+    the float32 path)."""
+    pkv = _pkv()
+    if kind == "decode":
+        H, Hkv, D, ctx = FUSED_CASES[0]
+        b = _batch("pinnedout_dec", H, Hkv, D, [1] * len(ctx), [c - 1 for c in ctx])
+    elif kind == "mixed":
+        H, Hkv, D, qlens, ncs = FUSED_MIXED_CASES[1]
+        b = _batch("pinnedout_mix", H, Hkv, D, qlens, ncs)
+    else:
+        b = _batch("pinnedout_f32", 4, 2, 64, [1, 7, 1], [39, 0, 19], dtype=torch.float32)
+    host_out = torch.full(tuple(b.q.shape), float("nan"), dtype=b.q.dtype).pin_memory()
+    if not host_buffer_is_device_mapped(host_out):
+        pytest.skip("pinned host memory is not device-mapped at its host address here")
+    kc0, vc0 = b.key_cache.clone(), b.value_cache.clone()
+    dev_out, ws = _fused(b)
+    torch.cuda.synchronize()
+    assert pkv.read_error_word(ws) == 0
+    b.key_cache.copy_(kc0)
+    b.value_cache.copy_(vc0)
+    ws2 = pkv.new_workspace(b.R, b.H, b.D)
+    got = pkv.reshape_and_cache_paged_attention(
+        b.k_new, b.v_new, b.slot_mapping, b.q, b.key_cache, b.value_cache, b.block_table,
+        b.qsl, b.seq_lens, b.nc, 1.0 / math.sqrt(b.D), out=host_out, workspace=ws2,
+        max_query_len=int(b.query_len.max()))
+    torch.cuda.synchronize()
+    assert got is host_out
+    assert pkv.read_error_word(ws2) == 0
+    assert torch.equal(host_out, dev_out.cpu())
+    compare(host_out, b.oracle(), b.qsl_host, b.dtype)
