@@ -291,3 +291,36 @@ def test_fused_step_writes_out_into_pinned_host_memory(kind):
     assert pkv.read_error_word(ws2) == 0
     assert torch.equal(host_out, dev_out.cpu())
     compare(host_out, b.oracle(), b.qsl_host, b.dtype)
+
+
+def test_prepared_call_config2_into_pinned_host_memory():
+    """The end-to-end step as bench.py times it: the Llama-3-8B decode batch
+    (64 requests, contexts 128-4096) through the binding's prepared call,
+    with out in pinned host memory, called twice in a row (the second call
+    writes the same new rows again); both results against the oracle."""
+    pkv = _pkv()
+    cfg = configs.decode_batch_llama8b()
+    b = Batch(cfg.kv, cfg.blocks, cfg.num_blocks, np.ones(len(cfg.context), np.int64),
+              cfg.context - 1, cfg.q, cfg.num_heads, cfg.dtype).alloc_cache().fill_history()
+    b.upload_metadata()
+    k, v, _ = b.new_tokens()
+    b.k_new, b.v_new = k.to("cuda", b.dtype), v.to("cuda", b.dtype)
+    host_out = torch.full(tuple(b.q.shape), float("nan"), dtype=b.q.dtype).pin_memory()
+    if not host_buffer_is_device_mapped(host_out):
+        pytest.skip("pinned host memory is not device-mapped at its host address here")
+    ws = pkv.new_workspace(b.R, b.H, b.D)
+    call = pkv.prepare_reshape_and_cache_paged_attention(
+        b.k_new, b.v_new, b.slot_mapping, b.q, b.key_cache, b.value_cache, b.block_table, b.qsl,
+        b.seq_lens, b.nc, 1.0 / math.sqrt(b.D), out=host_out, workspace=ws, max_query_len=1)
+    ref = b.oracle()
+    first = call()
+    torch.cuda.synchronize()
+    assert first is host_out
+    assert pkv.read_error_word(ws) == 0
+    compare(host_out, ref, b.qsl_host, b.dtype)
+    saved = host_out.clone()
+    host_out.fill_(float("nan"))
+    call()
+    torch.cuda.synchronize()
+    assert pkv.read_error_word(ws) == 0
+    assert torch.equal(host_out, saved)
