@@ -257,7 +257,8 @@ def build_decode_steps(pkv, device, replicas=4):
 
 
 def build_mixed_step(pkv, device, with_prefill_alone=False, **mix):
-    """The mixed chunked-prefill step (config 3 by default, or the mix the
+    """The mixed chunked-prefill step (the 512-token chunk at [1536, 2048)
+    beside 256 decodes by default, or the mix the
     keyword arguments of configs.mixed_chunked_step give) as one fused call,
     the same step's decodes alone and, on request, its prefill request
     alone."""
@@ -479,7 +480,7 @@ def event_time(fn, n, stream):
 
 
 def build_long_decode(pkv, device, pool=1 << 20):
-    """Config 4's decode call: 8 decodes over 131072-token histories,
+    """The long-context decode call: 8 decodes over 131072-token histories,
     Llama-3-70B heads (64/8/128), blocks scattered over a pool of `pool`
     blocks (2^20 = 68.7 GB by default); only the used blocks are filled.
     Returns the caches, the step and the generator that filled them (later
@@ -506,14 +507,14 @@ def build_long_decode(pkv, device, pool=1 << 20):
 
 def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     """Supporting measurements beside the headline: the long-context decode
-    (config 4), the continuous-batching trace (config 5) per step,
+    (8 x 131072-token histories), the 300-step continuous-batching trace per step,
     reshape_and_cache at 8192 tokens with and without the fused RoPE of Q and
     K, and the prefill kernel on a 2048-token prompt, on 8 such prompts in one
     call and on one 16384-token prompt."""
     from workloads import configs, trace_spec, generate_arrivals
     from workloads.generators import random_block_placement
     res = {}
-    # ---- config 4: 8 decodes over 131072-token histories, 2^20-block pool ----
+    # ---- long-context decode: 8 decodes over 131072-token histories, 2^20-block pool ----
     kc, vc, step, g = build_long_decode(pkv, device)
     for _ in range(3):
         step.attn()
@@ -822,7 +823,7 @@ def extra_measurements(pkv, device, stream, hbm_peak, bf16_peak):
     }
     del kc, vc, ws, sched
     torch.cuda.empty_cache()
-    # ---- config 5: the trace, per step (C++ scheduler, device-random K/V/Q) ----
+    # ---- the 300-step trace, per step (C++ scheduler, device-random K/V/Q) ----
     spec = trace_spec()
     H, Hkv, D, B = spec.num_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
     sched = pkv.Scheduler(spec.max_num_seqs, spec.max_num_batched_tokens, spec.chunk_size,
@@ -1038,7 +1039,7 @@ def main():
                     help="only --steps reshape_and_cache calls of 8192 tokens (4 rotating "
                          "batches), for ncu")
     ap.add_argument("--profile-long-decode", action="store_true",
-                    help="only --steps decode calls of config 4's requests (8 x 131072-token "
+                    help="only --steps calls of the long-context decode (8 x 131072-token "
                          "contexts, Llama-3-70B heads) in a pool that just holds them "
                          "(66560 blocks, 4.4 GB), for ncu")
     ap.add_argument("--profile-copy", action="store_true",

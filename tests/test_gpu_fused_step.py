@@ -78,7 +78,7 @@ def _check_against_two_calls(b):
     compare(fused_out, b.oracle(), b.qsl_host, b.dtype)
 
 
-def test_fused_decode_config2_llama8b():
+def test_fused_decode_llama8b_64_requests():
     cfg = configs.decode_batch_llama8b()
     b = Batch(cfg.kv, cfg.blocks, cfg.num_blocks, np.ones(len(cfg.context), np.int64),
               cfg.context - 1, cfg.q, cfg.num_heads, cfg.dtype).alloc_cache().fill_history()
@@ -293,7 +293,7 @@ def test_fused_step_writes_out_into_pinned_host_memory(kind):
     compare(host_out, b.oracle(), b.qsl_host, b.dtype)
 
 
-def test_prepared_call_config2_into_pinned_host_memory():
+def test_prepared_call_llama8b_decode_into_pinned_host_memory():
     """The end-to-end step as bench.py times it: the Llama-3-8B decode batch
     (64 requests, contexts 128-4096) through the binding's prepared call,
     with out in pinned host memory, called twice in a row (the second call

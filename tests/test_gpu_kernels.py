@@ -320,14 +320,14 @@ def _decode_cfg_batch(cfg):
                  cfg.context - 1, cfg.q, cfg.num_heads, cfg.dtype)
 
 
-def test_config2_decode_llama8b():
+def test_decode_llama8b_64_requests():
     cfg = configs.decode_batch_llama8b()
     b = _decode_cfg_batch(cfg).alloc_cache().fill_history().upload_metadata().write_new_tokens()
     out = b.attention()
     compare(out, b.oracle(), b.qsl_host, torch.bfloat16)
 
 
-def test_config3_mixed_chunked_step():
+def test_mixed_chunk512_beside_256_decodes():
     cfg = configs.mixed_chunked_step()
     b = Batch(cfg.kv, cfg.blocks, cfg.num_blocks, cfg.query_len, cfg.num_computed, cfg.q,
               cfg.num_heads, cfg.dtype).alloc_cache().fill_history().upload_metadata()
@@ -341,7 +341,7 @@ def test_config3_mixed_chunked_step():
 
 
 @pytest.mark.slow
-def test_config4_long_decode_llama70b():
+def test_long_decode_llama70b_8x131072():
     cfg = configs.long_decode_llama70b()
     b = _decode_cfg_batch(cfg).alloc_cache().fill_history().upload_metadata().write_new_tokens()
     out = b.attention()

@@ -65,7 +65,7 @@ def _history(name: str, lengths, hkv: int, d: int, dtype) -> KVHistory:
 
 
 # ---------------------------------------------------------------------------
-# config 1: tiny fp32 correctness case
+# tiny fp32 correctness case
 # ---------------------------------------------------------------------------
 @dataclass
 class TinyCase:
@@ -148,7 +148,7 @@ def long_decode_llama70b(num_reqs: int = 8, context: int = 131072, pool: int = 1
 
 
 # ---------------------------------------------------------------------------
-# config 3: mixed chunked-prefill step
+# mixed chunked-prefill step
 # ---------------------------------------------------------------------------
 @dataclass
 class MixedStep:
@@ -195,7 +195,7 @@ def mixed_chunked_step(num_decodes: int = 256, chunk_start: int = 1536, chunk_en
 
 
 # ---------------------------------------------------------------------------
-# config 5: continuous-batching trace parameters
+# continuous-batching trace parameters
 # ---------------------------------------------------------------------------
 @dataclass
 class TraceSpec:
